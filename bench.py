@@ -1,0 +1,459 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV cache decode step on GB300.
+
+One step = copy_blocks of the workload's copy-on-write pairs (when it has
+any) + paged_kv_append of the step's new tokens + paged_attention_decode over
+every sequence.  The default workload is the Llama-3-8B-class layer (64
+sequences, 32 query / 8 KV heads, bf16, block 16, contexts uniform in
+[512, 4096]); ``--workload`` selects another one.
+
+Metric: K/V bytes of the attended contexts per second (GB/s) and sequences per
+second; the roofline object reports paged_attention_decode's algorithmic
+bytes per launch over its CUDA-event time against the measured HBM peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Under torchrun (N > 1) every rank runs its own batch (different seed) with no
+data exchange; timing is the max over ranks and value aggregates all ranks.
+``--impl reference`` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); sequences/s per step"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = ROOT / "profiles" / "traffic_per_launch.txt"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-seqs", type=int, default=0, help="0: the whole batch")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws: int, backend: str):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_seed(base: int, rank: int) -> int:
+    return base ^ (0x1000193 * rank) if rank else base
+
+
+# ---------------------------------------------------------------- peaks, clocks, traffic
+def measured_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return json.loads(p.read_text())
+        except Exception:
+            pass
+    return {}
+
+
+def traffic_per_launch(workload: str):
+    """dram read+write bytes per decode launch from the committed ncu summary, if it
+    still describes the current kernel (same source hash)."""
+    if not TRAFFIC_FILE.exists():
+        return None
+    import hashlib
+    src = (ROOT / "paged_kv_cache_11_gb300" / "csrc" / "decode.cu").read_bytes()
+    h = hashlib.sha256(src).hexdigest()[:16]
+    for line in TRAFFIC_FILE.read_text().splitlines():
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == workload and parts[1] == h:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        lo, hi = (self.t0 or 0) - 0.15, (self.t1 or time.time()) + 0.15
+        rows = [s for t, s in self.samples if lo <= t <= hi] or [s for _, s in self.samples[-3:]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload description
+def describe(wl) -> dict:
+    s = wl.spec
+    d = {"workload": s.name, "num_seqs": wl.num_seqs, "num_q_heads": s.num_q_heads,
+         "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size, "dtype": s.dtype,
+         "context_lens": {"min": int(wl.context_lens.min()), "max": int(wl.context_lens.max()),
+                          "mean": float(wl.context_lens.mean())},
+         "pool_blocks": wl.num_blocks, "appended_tokens": int(len(wl.slot_mapping)),
+         "cow_pairs": int(len(wl.cow_pairs)), "kv_bytes_per_step": wl.kv_bytes()}
+    if s.groups:
+        d["unique_kv_bytes_per_step"] = wl.unique_kv_bytes()
+    return d
+
+
+def decode_algorithmic_bytes(wl) -> int:
+    """Bytes paged_attention_decode must move: the attended K/V, q, the block-table
+    entries it reads, context_lens and the fp32 output."""
+    bs = wl.block_size
+    blocks = int(((wl.context_lens.astype(np.int64) + bs - 1) // bs).sum())
+    q = wl.num_seqs * wl.num_q_heads * wl.head_dim * 2
+    out = wl.num_seqs * wl.num_q_heads * wl.head_dim * 4
+    return wl.kv_bytes() + q + out + blocks * 4 + wl.num_seqs * 4
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def time_oracle(wl, nseq: int, threads: int):
+    """One oracle step (copy + append + decode) over the first nseq sequences; returns
+    (seconds, kv_bytes, sequences)."""
+    import oracle
+    nseq = min(nseq or wl.num_seqs, wl.num_seqs)
+    sel = [(s, h) for s in range(nseq) for h in range(wl.num_q_heads)]
+    kc, vc = wl.k_cache, wl.v_cache  # the oracle writes the same bytes the GPU step writes
+    t0 = time.perf_counter()
+    if len(wl.cow_pairs):
+        oracle.copy_blocks(kc, vc, wl.cow_pairs)
+    if len(wl.slot_mapping):
+        m = wl.append_seq < nseq
+        oracle.append(np.ascontiguousarray(wl.new_k[m]), np.ascontiguousarray(wl.new_v[m]), wl.slot_mapping[m], kc, vc)
+    oracle.decode(wl.q, kc, vc, wl.block_tables, wl.context_lens, wl.scale, wl.dtype, select=sel, threads=threads)
+    dt = time.perf_counter() - t0
+    kvb = int(wl.context_lens[:nseq].astype(np.int64).sum()) * 2 * wl.num_kv_heads * wl.head_dim * 2
+    return dt, kvb, nseq
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from paged_kv_cache_11_gb300 import _build, workload as W
+    import oracle
+    _build.build_generator()
+    oracle.build()
+    wl = W.make_workload(args.workload)
+    threads = host_threads()
+    nseq = args.cpu_sample_seqs
+    if not nseq:
+        # size each step's sample so that warmup + steps take about a minute
+        t1, _, _ = time_oracle(wl, 1, threads)
+        per_step = 60.0 / max(1, args.steps + args.warmup)
+        nseq = int(max(1, min(wl.num_seqs, 8, per_step // max(t1, 1e-6))))
+    for _ in range(max(0, args.warmup)):
+        time_oracle(wl, nseq, threads)
+    tot, kvb, seqs = 0.0, 0, 0
+    for _ in range(args.steps):
+        dt, b, n = time_oracle(wl, nseq, threads)
+        tot += dt
+        kvb += b
+        seqs += n
+    gbs = kvb / tot / 1e9
+    sample = f"first {nseq} of {wl.num_seqs} sequences per step (all their query heads), {args.steps} steps"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": describe(wl), "seq_per_s": seqs / tot,
+        "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    import paged_kv_cache_11_gb300 as pkv
+    from paged_kv_cache_11_gb300 import _build, workload as W
+
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(ws, "nccl")
+    _build.build_all()
+    pkv.binding._lib()
+
+    spec = W.SPECS[args.workload]
+    wl = W.make_workload(args.workload, seed=rank_seed(W.default_seed(spec), rank))
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[wl.dtype]
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(dt)
+
+    kc, vc = up(wl.k_cache), up(wl.v_cache)
+    q, nk, nv = up(wl.q), up(wl.new_k), up(wl.new_v)
+    sm = torch.from_numpy(wl.slot_mapping).to(dev)
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    cl = torch.from_numpy(wl.context_lens).to(dev)
+    cow = torch.from_numpy(wl.cow_pairs).to(dev) if len(wl.cow_pairs) else None
+    out = torch.empty((wl.num_seqs, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
+    mcl = wl.max_context_len
+    need = pkv.paged_attention_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, mcl, args.partition_size)
+    wsp = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if cow is not None:
+            pkv.copy_blocks(kc, vc, cow)
+        if len(wl.slot_mapping):
+            pkv.paged_kv_append(nk, nv, sm, kc, vc)
+        if ev is not None:
+            ev[0].record(stream)
+        pkv.paged_attention_decode(q, kc, vc, bt, cl, wl.scale, out=out, max_context_len=mcl,
+                                   partition_size=args.partition_size, workspace=wsp)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert pkv.check_device_error() == 0
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark(True)
+    l0 = pkv.launch_count()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = pkv.launch_count() - l0
+    if clocks:
+        clocks.mark(False)
+    if dist:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in evs]
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    assert pkv.check_device_error() == 0
+
+    # ---- end to end: host buffers in, result out, through the public API
+    pin = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(dt).pin_memory()
+    h_q, h_nk, h_nv = pin(wl.q), pin(wl.new_k), pin(wl.new_v)
+    h_sm = torch.from_numpy(wl.slot_mapping).pin_memory()
+    h_bt = torch.from_numpy(wl.block_tables).pin_memory()
+    h_cl = torch.from_numpy(wl.context_lens).pin_memory()
+    h_cow = torch.from_numpy(wl.cow_pairs).pin_memory() if cow is not None else None
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_nk, h_nv, h_sm, h_bt, h_cl) + ((h_cow,) if h_cow is not None else ()))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        q.copy_(h_q, non_blocking=True)
+        nk.copy_(h_nk, non_blocking=True)
+        nv.copy_(h_nv, non_blocking=True)
+        sm.copy_(h_sm, non_blocking=True)
+        bt.copy_(h_bt, non_blocking=True)
+        cl.copy_(h_cl, non_blocking=True)
+        if h_cow is not None:
+            cow.copy_(h_cow, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 500))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    assert pkv.check_device_error() == 0
+
+    # ---- aggregate over ranks
+    kvb = float(wl.kv_bytes())
+    ms_max = max_over_ranks(dist, ms_total, dev)
+    e2e_max = max_over_ranks(dist, e2e_ms, dev)
+    kv_all = sum_over_ranks(dist, kvb, dev)
+    seqs_all = sum_over_ranks(dist, float(wl.num_seqs), dev)
+    launches_all = int(sum_over_ranks(dist, float(launches), dev))
+    clk = clocks.stop() if clocks else None
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peaks = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    steps = args.steps
+    value = kv_all * steps / (ms_max / 1e3) / 1e9
+    dec_bytes = decode_algorithmic_bytes(wl)
+    achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
+    traffic = traffic_per_launch(args.workload)
+
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        threads = host_threads()
+        t, b, n = time_oracle(wl, args.cpu_sample_seqs, threads)
+        cpu = {"value": b / t / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"one step over the first {n} of {wl.num_seqs} sequences (all query heads), "
+                         f"{t:.2f} s on {threads} host threads"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": ms_max / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype, "data": "synthetic",
+        "config": {**describe(wl), "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": f"inputs larger than L2 ({wl.kv_bytes() / 1e6:.0f} MB of K/V vs 129 MB), no flush",
+                   "partition_size": args.partition_size or 512},
+        "seq_per_s": seqs_all * steps / (ms_max / 1e3),
+        "pct_of_hbm_peak": 100.0 * value / peak,
+        "roofline": {"kernel": "paged_attention_decode (decode kernel + split-K merge)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_src, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_avg_ms},
+        "e2e": {"value": kv_all * e2e_steps / (e2e_max / 1e3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches_all,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

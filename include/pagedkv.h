@@ -1,0 +1,198 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: the decode hot path of a paged KV
+ * cache on one GPU (sm_103a).
+ *
+ * What the operations are (web pages on paged KV caches; page title, then
+ * section):
+ *   - tonho.wtf "vllm", "como funciona": the KV cache of a sequence is cut
+ *     into fixed-size blocks (16 tokens by default) that are slices of one
+ *     GPU pool; a per-sequence block table maps logical blocks to physical
+ *     ones; a new physical block is taken only when the last one is full;
+ *     decode attention takes the current token's query against the keys of
+ *     one block at a time and accumulates the output against that block's
+ *     values, so blocks need not be adjacent; sequences share blocks through
+ *     reference counts, and a write into the last shared block copies that
+ *     block and only it.
+ *   - tonho.wtf "vllm", "o que isso custou": the three kernels the method
+ *     needs -- block write, paged read fused with attention, batched block
+ *     copy.  They are paged_kv_append, paged_attention_decode and
+ *     copy_blocks below.
+ *   - techtrendfeed "KV Cache Administration: PagedAttention &
+ *     RadixAttention", "How PagedAttention Works", steps 1-4 (blocks of 16
+ *     or 32 tokens; block table used by the kernel to gather K and V; growth
+ *     one block at a time; copy-on-write), and "Why this modified LLM
+ *     serving" (paging changes neither the attention result nor the model's
+ *     outputs).
+ *
+ * Conventions shared by every call:
+ *   - Cache layout: k_cache and v_cache are each
+ *       [num_blocks][num_kv_heads][block_size][head_dim]
+ *     row-major, elements of pkv_cache_desc.dtype.  Token position t of a
+ *     sequence sits in logical block t / block_size at offset
+ *     t % block_size; the (block, KV head) tile is contiguous.
+ *   - A slot is physical_block * block_size + offset.
+ *   - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   - Ownership: every data pointer is a caller-owned DEVICE pointer unless
+ *     stated otherwise; the library keeps no pointer after a call returns,
+ *     allocates no memory, and never synchronises except in
+ *     pkv_check_device_error.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *     default stream).  Every call is asynchronous on it.
+ *   - Errors found on the host (null or misaligned pointers, unsupported
+ *     shapes, too small a workspace) return a status and launch nothing.
+ *     Bad metadata that lives on the device (a slot, block id or context
+ *     length outside the pool) never faults: the kernel skips the access,
+ *     zero-fills the affected output, and records the first such error in a
+ *     per-device error word that pkv_check_device_error reads and clears.
+ *   - Kernels never wait on another kernel or CTA.  Waits inside one CTA
+ *     (its copy pipeline) are bounded; a wait that runs out records
+ *     PKV_DEVERR_TIMEOUT and the CTA returns.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,     /* null/misaligned pointer or bad size */
+    PKV_ERR_UNSUPPORTED = 2,     /* valid but not implemented shape or dtype */
+    PKV_ERR_WORKSPACE = 3,       /* workspace missing or too small */
+    PKV_ERR_CUDA = 4,            /* a CUDA runtime or driver call failed */
+    PKV_ERR_DEVICE_METADATA = 5  /* reported by pkv_check_device_error */
+} pkv_status;
+
+typedef enum { PKV_BF16 = 0, PKV_FP16 = 1, PKV_FP32 = 2 } pkv_dtype;
+
+/* Codes stored in the device error word (first error wins). */
+enum {
+    PKV_DEVERR_NONE = 0,
+    PKV_DEVERR_SLOT = 1,        /* append: slot >= num_blocks * block_size */
+    PKV_DEVERR_COPY_ID = 2,     /* copy_blocks: src or dst outside the pool */
+    PKV_DEVERR_CONTEXT_LEN = 3, /* decode: context_lens[s] < 0, above the table's capacity, or above max_context_len */
+    PKV_DEVERR_BLOCK_ID = 4,    /* decode: block_tables entry outside the pool */
+    PKV_DEVERR_TIMEOUT = 5      /* a bounded in-CTA wait ran out */
+};
+
+/* Shape of one layer's paged cache (host struct, read during the call). */
+typedef struct {
+    int64_t num_blocks;  /* physical blocks in the pool, >= 1 */
+    int32_t num_kv_heads;
+    int32_t block_size;  /* tokens per block: 16 or 32 */
+    int32_t head_dim;    /* 128 */
+    int32_t dtype;       /* pkv_dtype: PKV_BF16 or PKV_FP16 */
+} pkv_cache_desc;
+
+/* Human-readable name of a status. Never NULL. */
+const char* pkv_status_string(pkv_status status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int pkv_version(void);
+
+/*
+ * Block write ("vllm", "como funciona" and "o que isso custou").
+ * For every token t with slot_mapping[t] >= 0 and every KV head h:
+ *     k_cache[slot / bs][h][slot % bs][:] = k[t][h][:]   (same for v)
+ * k, v:          [num_tokens][num_kv_heads][head_dim], cache dtype, 16-byte
+ *                aligned device memory.
+ * slot_mapping:  [num_tokens] int64 device memory; a negative slot marks a
+ *                padding token, which is skipped.
+ * k_cache, v_cache: the pool (layout above), 16-byte aligned.
+ * num_tokens == 0 is a no-op.  Two tokens with the same slot race (last
+ * writer undefined).  A slot >= num_blocks * block_size is skipped and
+ * recorded as PKV_DEVERR_SLOT.  The copy is bit-exact.
+ */
+pkv_status paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                           void* k_cache, void* v_cache, const pkv_cache_desc* cache, void* stream);
+
+/*
+ * Bytes of workspace paged_attention_decode needs for these sizes (0 when
+ * the call runs in a single pass).  partition_size as for
+ * paged_attention_decode (0 = automatic).  Returns 0 for invalid sizes.
+ */
+size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                       int32_t max_context_len, int32_t partition_size);
+
+/*
+ * Paged decode attention ("vllm", "como funciona": the query of the current
+ * token against the keys of one block at a time, output accumulated against
+ * the same block's values; blocks need not be adjacent).
+ * For every sequence s and query head h, with L = context_lens[s] and
+ * kvh = h / (num_q_heads / num_kv_heads):
+ *     out[s][h][:] = sum_{t<L} softmax_t(scale * q[s][h] . K[t]) V[t]
+ * where K[t], V[t] are row t % bs of tile (block_tables[s][t / bs], kvh).
+ * L counts every attended token, including the one appended this step;
+ * L == 0 gives zeros.
+ *
+ * q:               [num_seqs][num_q_heads][head_dim], cache dtype, 16-byte aligned.
+ * k_cache, v_cache: the pool, 16-byte aligned.
+ * block_tables:    [num_seqs][max_blocks_per_seq] int32; entries past
+ *                  ceil(L / bs) are never read.
+ * context_lens:    [num_seqs] int32, each in [0, min(max_context_len,
+ *                  max_blocks_per_seq * bs)].
+ * max_context_len: host-side upper bound of context_lens; it sizes the
+ *                  split-K partitions and the workspace.
+ * out:             [num_seqs][num_q_heads][head_dim] of out_dtype (PKV_FP32,
+ *                  PKV_BF16 or PKV_FP16), 16-byte aligned.
+ * partition_size:  tokens per split-K partition, a multiple of block_size;
+ *                  0 picks 512.  When max_context_len > partition_size each
+ *                  partition writes (o_p, lse_p) to the workspace and a
+ *                  second kernel merges them through their log-sum-exp;
+ *                  otherwise one kernel writes out directly.
+ * workspace:       device memory of at least
+ *                  paged_attention_workspace_bytes(...) bytes, 256-byte
+ *                  aligned (may be NULL when that is 0).  Contents on entry
+ *                  are ignored.
+ * Supported: head_dim 128; block_size 16 or 32; bf16 or fp16 caches;
+ * num_q_heads a multiple of num_kv_heads; num_seqs <= 65535.
+ * Results depend only on logical token order: permuting physical block ids
+ * leaves the output bit-for-bit unchanged.
+ */
+pkv_status paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_context_len, float scale, void* out, int32_t out_dtype,
+                                  const pkv_cache_desc* cache, int32_t partition_size, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
+ * Batched copy-on-write block copy ("vllm", "como funciona": a write into
+ * the last shared block copies that block and only it; "o que isso
+ * custou": batched block copy).
+ * For each pair i and each layer l:
+ *     k_caches[l][dst] = k_caches[l][src], v_caches[l][dst] = v_caches[l][src]
+ * (whole blocks: every KV head and slot), with (src, dst) =
+ * (src_dst_pairs[2i], src_dst_pairs[2i+1]).
+ * k_caches, v_caches: HOST arrays of num_layers device pointers (each
+ *                  16-byte aligned), all layers of the shape in `cache`.
+ * src_dst_pairs:   [num_pairs][2] int64 DEVICE memory.
+ * Destinations must be distinct and no destination may also be a source
+ * (otherwise the result depends on block scheduling); an id outside the
+ * pool skips that pair and records PKV_DEVERR_COPY_ID.  Bit-exact.
+ */
+pkv_status copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                       const int64_t* src_dst_pairs, int32_t num_pairs, const pkv_cache_desc* cache,
+                       void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns PKV_OK (and *first_error_code = 0) when no kernel recorded
+ * an error since the last check, PKV_ERR_DEVICE_METADATA with the first
+ * PKV_DEVERR_* code otherwise, or PKV_ERR_CUDA.  first_error_code may be
+ * NULL.
+ */
+pkv_status pkv_check_device_error(void* stream, int32_t* first_error_code);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t pkv_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,279 @@
+// api.cu -- the C ABI declared in include/pagedkv.h: argument checks on the
+// host, TMA descriptor encoding, the per-device error word, and dispatch to
+// the kernels in decode.cu and append_copy.cu.
+#include <climits>
+#include <cstring>
+#include <atomic>
+#include <mutex>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+// First device-side error since the last pkv_check_device_error, per device.
+static __device__ int g_pkv_error = 0;
+
+static std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_err_mutex;
+static int* g_err_ptr[kMaxDevices] = {};
+
+// Device address of this device's error word (looked up once per device).
+static int* error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_err_mutex);
+    if (!g_err_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_pkv_error) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<int*>(ptr);
+    }
+    return g_err_ptr[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// The pool viewed as a 2-D tensor [num_blocks * Hkv * bs rows][128 columns];
+// box = one 64-column half of a (block, KV head) tile, 128-byte swizzle.
+static pkv_status encode_cache_map(CUtensorMap* m, const void* base, const pkv_cache_desc& c) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return PKV_ERR_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)c.num_blocks * c.num_kv_heads * c.block_size};
+    const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)c.block_size};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r =
+        fn(m, c.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_INVALID_ARG;
+}
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Shape checks common to every call on a cache.
+static pkv_status check_cache(const pkv_cache_desc* c) {
+    if (!c) return PKV_ERR_INVALID_ARG;
+    if (c->num_blocks < 1 || c->num_kv_heads < 1 || c->block_size < 1 || c->head_dim < 1) return PKV_ERR_INVALID_ARG;
+    if (c->dtype != PKV_BF16 && c->dtype != PKV_FP16) return PKV_ERR_UNSUPPORTED;
+    if ((c->head_dim * 2) % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+static int resolve_partition(int32_t partition_size) { return partition_size == 0 ? kAutoPartition : partition_size; }
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+        case PKV_ERR_CUDA: return "CUDA call failed";
+        case PKV_ERR_DEVICE_METADATA: return "device-side metadata error";
+    }
+    return "unknown status";
+}
+
+int pkv_version(void) { return 100; }
+
+uint64_t pkv_launch_count(void) { return g_launches.load(); }
+
+pkv_status paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                           void* k_cache, void* v_cache, const pkv_cache_desc* cache, void* stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return PKV_ERR_INVALID_ARG;
+    const int row_vecs = cache->head_dim * 2 / 16;
+    const int64_t total = num_tokens * cache->num_kv_heads * row_vecs;
+    if (total / num_tokens != (int64_t)cache->num_kv_heads * row_vecs || (total + 255) / 256 > INT_MAX)
+        return PKV_ERR_INVALID_ARG;
+    int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+    AppendParams p;
+    p.err = err;
+    p.k = static_cast<const uint4*>(k);
+    p.v = static_cast<const uint4*>(v);
+    p.slot_mapping = slot_mapping;
+    p.k_cache = static_cast<uint4*>(k_cache);
+    p.v_cache = static_cast<uint4*>(v_cache);
+    p.num_tokens = num_tokens;
+    p.num_slots = cache->num_blocks * cache->block_size;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.block_size = cache->block_size;
+    p.row_vecs = row_vecs;
+    int launches = 0;
+    const cudaError_t e = launch_append(p, static_cast<cudaStream_t>(stream), &launches);
+    g_launches += launches;
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                       int32_t max_context_len, int32_t partition_size) {
+    if (num_seqs < 0 || num_q_heads < 1 || head_dim < 1 || max_context_len < 0 || partition_size < 0) return 0;
+    const int64_t P = resolve_partition(partition_size);
+    const int64_t parts = max_context_len == 0 ? 1 : (max_context_len + P - 1) / P;
+    if (parts <= 1) return 0;
+    const int64_t rows = (int64_t)num_seqs * num_q_heads * parts;
+    const int64_t o_bytes = ((rows * head_dim * 4) + 255) / 256 * 256;
+    const int64_t lse_bytes = ((rows * 4) + 255) / 256 * 256;
+    return (size_t)(o_bytes + lse_bytes);
+}
+
+pkv_status paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_context_len, float scale, void* out, int32_t out_dtype,
+                                  const pkv_cache_desc* cache, int32_t partition_size, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (cache->head_dim != kHeadDim) return PKV_ERR_UNSUPPORTED;
+    if (cache->block_size != 16 && cache->block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || num_seqs > 65535 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (out_dtype != PKV_FP32 && out_dtype != PKV_BF16 && out_dtype != PKV_FP16) return PKV_ERR_INVALID_ARG;
+    if (max_blocks_per_seq < 1 || max_context_len < 0 ||
+        (int64_t)max_blocks_per_seq * cache->block_size > INT_MAX ||
+        max_context_len > (int64_t)max_blocks_per_seq * cache->block_size)
+        return PKV_ERR_INVALID_ARG;
+    if (partition_size < 0 || (partition_size > 0 && partition_size % cache->block_size != 0))
+        return PKV_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PKV_ERR_INVALID_ARG;
+    // tile rows must be addressable by a 32-bit TMA coordinate
+    if (cache->num_blocks * cache->num_kv_heads * cache->block_size > INT_MAX) return PKV_ERR_UNSUPPORTED;
+    const int group = num_q_heads / cache->num_kv_heads;
+    const int head_tiles = (group + kHeadTile - 1) / kHeadTile;
+    if ((int64_t)cache->num_kv_heads * head_tiles > 65535) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+
+    const int P = resolve_partition(partition_size);
+    const int max_parts = max_context_len == 0 ? 1 : (max_context_len + P - 1) / P;
+    const bool split = max_parts > 1;
+    const size_t need = paged_attention_workspace_bytes(num_seqs, num_q_heads, kHeadDim, max_context_len,
+                                                        partition_size);
+    if (split && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return PKV_ERR_WORKSPACE;
+
+    int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+    CUtensorMap tmk, tmv;
+    st = encode_cache_map(&tmk, k_cache, *cache);
+    if (st != PKV_OK) return st;
+    st = encode_cache_map(&tmv, v_cache, *cache);
+    if (st != PKV_OK) return st;
+
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = out;
+    if (split) {
+        const int64_t rows = (int64_t)num_seqs * num_q_heads * max_parts;
+        const int64_t o_bytes = ((rows * kHeadDim * 4) + 255) / 256 * 256;
+        p.part_o = static_cast<float*>(workspace);
+        p.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+    }
+    p.err = err;
+    p.num_blocks = cache->num_blocks;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.len_limit = max_context_len;  // already <= max_blocks_per_seq * block_size
+    p.partition_size = P;
+    p.max_parts = max_parts;
+    p.group = group;
+    p.head_tiles = head_tiles;
+    p.out_dtype = out_dtype;
+    p.split = split ? 1 : 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    int launches = 0;
+    const cudaError_t e =
+        launch_decode(p, cache->dtype, cache->block_size, tmk, tmv, static_cast<cudaStream_t>(stream), &launches);
+    g_launches += launches;
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                       const int64_t* src_dst_pairs, int32_t num_pairs, const pkv_cache_desc* cache,
+                       void* stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (num_layers < 0 || num_pairs < 0) return PKV_ERR_INVALID_ARG;
+    if (num_layers == 0 || num_pairs == 0) return PKV_OK;
+    if (!k_caches || !v_caches || !src_dst_pairs || !aligned(src_dst_pairs, 8)) return PKV_ERR_INVALID_ARG;
+    for (int l = 0; l < num_layers; ++l)
+        if (!k_caches[l] || !v_caches[l] || !aligned(k_caches[l], 16) || !aligned(v_caches[l], 16))
+            return PKV_ERR_INVALID_ARG;
+    const int64_t block_bytes = (int64_t)cache->num_kv_heads * cache->block_size * cache->head_dim * 2;
+    if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    const int64_t block_vecs = block_bytes / 16;
+    if ((block_vecs + 4095) / 4096 > 65535) return PKV_ERR_UNSUPPORTED;
+    int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+    int launches = 0;
+    cudaError_t e = cudaSuccess;
+    for (int l0 = 0; l0 < num_layers && e == cudaSuccess; l0 += kCopyMaxLayers) {
+        CopyParams p;
+        std::memset(&p, 0, sizeof(p));
+        p.err = err;
+        p.num_layers = num_layers - l0 < kCopyMaxLayers ? num_layers - l0 : kCopyMaxLayers;
+        for (int l = 0; l < p.num_layers; ++l) {
+            p.k[l] = static_cast<uint4*>(k_caches[l0 + l]);
+            p.v[l] = static_cast<uint4*>(v_caches[l0 + l]);
+        }
+        p.pairs = src_dst_pairs;
+        p.num_blocks = cache->num_blocks;
+        p.block_vecs = block_vecs;
+        p.num_pairs = num_pairs;
+        e = launch_copy_blocks(p, static_cast<cudaStream_t>(stream), &launches);
+    }
+    g_launches += launches;
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_check_device_error(void* stream, int32_t* first_error_code) {
+    if (first_error_code) *first_error_code = 0;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PKV_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_pkv_error, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
+    if (v == 0) return PKV_OK;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_pkv_error, &zero, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
+    if (first_error_code) *first_error_code = v;
+    return PKV_ERR_DEVICE_METADATA;
+}
+
+}  // extern "C"

@@ -1,0 +1,208 @@
+// pkv_internal.cuh -- internal declarations shared by the library's
+// translation units: launch parameter blocks, launcher entry points, the
+// per-device error word and thin inline-PTX wrappers (mbarrier, TMA,
+// ldmatrix, mma.sync) for sm_103a.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pagedkv.h"
+
+namespace pkv {
+
+constexpr int kHeadDim = 128;          // supported head_dim
+constexpr int kAutoPartition = 512;    // tokens per split-K partition when the caller passes 0
+constexpr int kHeadTile = 16;          // query heads of one GQA group handled by one CTA (mma M)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on any in-CTA wait (2 s)
+
+// The per-device error word lives in the API translation unit; kernels get
+// its device address as a parameter.  First error wins (atomicCAS from 0).
+__device__ __forceinline__ void record_error(int* err, int code) { atomicCAS(err, 0, code); }
+
+// ---------------------------------------------------------------------------
+// Launch parameters
+// ---------------------------------------------------------------------------
+struct DecodeParams {
+    const void* q;               // [B][Hq][D]
+    const int32_t* block_tables; // [B][max_blocks_per_seq]
+    const int32_t* context_lens; // [B]
+    void* out;                   // [B][Hq][D] of out_dtype
+    float* part_o;               // [B][Hq][max_parts][D]   (split only)
+    float* part_lse;             // [B][Hq][max_parts], log2 domain (split only)
+    int* err;                    // device error word
+    int64_t num_blocks;
+    int num_seqs, num_q_heads, num_kv_heads;
+    int max_blocks_per_seq;
+    int len_limit;               // min(max_context_len, max_blocks_per_seq * block_size)
+    int partition_size;          // tokens, multiple of block_size
+    int max_parts;               // ceil(max_context_len / partition_size), >= 1
+    int group;                   // G = Hq / Hkv
+    int head_tiles;              // ceil(G / kHeadTile)
+    int out_dtype;               // pkv_dtype
+    int split;                   // 1: sequences with > 1 partition write partials
+    float scale_log2;            // scale * log2(e)
+};
+
+// Host-side launchers (decode.cu); return a cudaError_t from the launch.
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int block_size, const CUtensorMap& tmk,
+                          const CUtensorMap& tmv, cudaStream_t stream, int* launches);
+
+struct AppendParams {
+    int* err;
+    const uint4* k;
+    const uint4* v;
+    const int64_t* slot_mapping;
+    uint4* k_cache;
+    uint4* v_cache;
+    int64_t num_tokens;
+    int64_t num_slots;   // num_blocks * block_size
+    int num_kv_heads, block_size, row_vecs;  // row_vecs = head_dim * elt / 16
+};
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream, int* launches);
+
+constexpr int kCopyMaxLayers = 64;
+struct CopyParams {
+    int* err;
+    uint4* k[kCopyMaxLayers];
+    uint4* v[kCopyMaxLayers];
+    const int64_t* pairs;
+    int64_t num_blocks;
+    int64_t block_vecs;  // 16-byte vectors per block of one cache
+    int num_layers, num_pairs;
+};
+cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream, int* launches);
+
+// ---------------------------------------------------------------------------
+// Inline PTX
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase of parity `parity` to complete; gives up after
+// kWaitLimitNs and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+// 2-D tiled TMA load into this CTA's shared memory, completion counted on
+// the mbarrier `bar` in bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D += A * B, m16n8k16, fp32 accumulate; A row-major 16x16, B col-major 16x8.
+template <bool kBF16>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (kBF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+// Pack two floats (lo in the low half) into a 16-bit pair, round to nearest
+// even; also return the value each element rounded to.
+template <bool kBF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, float& lo_r, float& hi_r) {
+    if constexpr (kBF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        lo_r = __low2float(v);
+        hi_r = __high2float(v);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        lo_r = __low2float(v);
+        hi_r = __high2float(v);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    float a, b;
+    return pack2<kBF16>(lo, hi, a, b);
+}
+
+}  // namespace pkv

@@ -1,0 +1,95 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every function include/pagedkv.h declares, and rejects bad arguments on the
+host before touching CUDA."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from paged_kv_cache_11_gb300 import _build, binding
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "pagedkv.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build_library()
+    return binding._lib()
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    return re.findall(r"^(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    assert {"paged_kv_append", "paged_attention_decode", "copy_blocks", "paged_attention_workspace_bytes",
+            "pkv_check_device_error", "pkv_status_string", "pkv_launch_count", "pkv_version"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_built_for_sm_103a_only():
+    src = (Path(_build.__file__)).read_text()
+    assert "arch=compute_103a,code=sm_103a" in src
+
+
+def test_status_strings(lib):
+    assert binding.status_string(0) == "ok"
+    assert binding.status_string(3).startswith("workspace")
+    assert binding.status_string(99) == "unknown status"
+    assert binding.version() >= 100
+
+
+def _desc(**kw):
+    d = dict(num_blocks=64, num_kv_heads=1, block_size=16, head_dim=128, dtype=binding.PKV_BF16)
+    d.update(kw)
+    return binding.CacheDesc(**d)
+
+
+def _decode(lib, desc, num_seqs=1, hq=4, max_ctx=16, out_dtype=binding.PKV_FP32, P=0, ws=None, ws_bytes=0,
+            maxb=4, ptr=16):
+    return lib.paged_attention_decode(ptr, ptr, ptr, ptr, maxb, ptr, num_seqs, hq, max_ctx, 0.1, ptr, out_dtype,
+                                      ctypes.byref(desc), P, ws, ws_bytes, None)
+
+
+def test_decode_host_validation(lib):
+    d = _desc()
+    assert _decode(lib, d, num_seqs=0) == binding.PKV_OK                     # no-op
+    assert _decode(lib, _desc(head_dim=64)) == binding.PKV_ERR_UNSUPPORTED
+    assert _decode(lib, _desc(block_size=8)) == binding.PKV_ERR_UNSUPPORTED
+    assert _decode(lib, _desc(dtype=binding.PKV_FP32)) == binding.PKV_ERR_UNSUPPORTED
+    assert _decode(lib, _desc(num_kv_heads=2), hq=3) == binding.PKV_ERR_INVALID_ARG
+    assert _decode(lib, d, max_ctx=65) == binding.PKV_ERR_INVALID_ARG         # above 4 blocks x 16
+    assert _decode(lib, d, P=24) == binding.PKV_ERR_INVALID_ARG               # not a multiple of 16
+    assert _decode(lib, d, out_dtype=7) == binding.PKV_ERR_INVALID_ARG
+    assert _decode(lib, d, ptr=18) == binding.PKV_ERR_INVALID_ARG             # misaligned pointers
+    assert _decode(lib, d, max_ctx=64, P=16) == binding.PKV_ERR_WORKSPACE     # split needs a workspace
+    assert _decode(lib, d, num_seqs=70000) == binding.PKV_ERR_INVALID_ARG
+
+
+def test_workspace_bytes(lib):
+    assert binding.paged_attention_workspace_bytes(8, 64, 128, 512, 0) == 0          # one partition
+    n = binding.paged_attention_workspace_bytes(8, 64, 128, 131072, 0)
+    rows = 8 * 64 * 256
+    assert n >= rows * 128 * 4 + rows * 4 and n % 256 == 0
+    assert binding.paged_attention_workspace_bytes(-1, 64, 128, 10, 0) == 0
+
+
+def test_append_and_copy_host_validation(lib):
+    d = _desc()
+    assert lib.paged_kv_append(16, 16, 16, 0, 16, 16, ctypes.byref(d), None) == binding.PKV_OK   # no tokens
+    assert lib.paged_kv_append(16, 16, 16, -1, 16, 16, ctypes.byref(d), None) == binding.PKV_ERR_INVALID_ARG
+    assert lib.paged_kv_append(None, 16, 16, 4, 16, 16, ctypes.byref(d), None) == binding.PKV_ERR_INVALID_ARG
+    assert lib.paged_kv_append(24, 16, 16, 4, 16, 16, ctypes.byref(d), None) == binding.PKV_ERR_INVALID_ARG
+    assert lib.paged_kv_append(16, 16, 16, 4, 16, 16, None, None) == binding.PKV_ERR_INVALID_ARG
+    arr = (ctypes.c_void_p * 1)(16)
+    assert lib.copy_blocks(arr, arr, 1, 16, 0, ctypes.byref(d), None) == binding.PKV_OK             # no pairs
+    bad = (ctypes.c_void_p * 1)(20)
+    assert lib.copy_blocks(bad, arr, 1, 16, 3, ctypes.byref(d), None) == binding.PKV_ERR_INVALID_ARG
+    assert lib.copy_blocks(arr, arr, -1, 16, 3, ctypes.byref(d), None) == binding.PKV_ERR_INVALID_ARG
