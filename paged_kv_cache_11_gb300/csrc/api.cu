@@ -170,7 +170,7 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
     // tile rows must be addressable by a 32-bit TMA coordinate
     if (cache->num_blocks * cache->num_kv_heads * cache->block_size > INT_MAX) return PKV_ERR_UNSUPPORTED;
     const int group = num_q_heads / cache->num_kv_heads;
-    const int head_tiles = (group + kHeadTile - 1) / kHeadTile;
+    const int head_tiles = (group + decode_head_tile(group) - 1) / decode_head_tile(group);
     if ((int64_t)cache->num_kv_heads * head_tiles > 65535) return PKV_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PKV_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;

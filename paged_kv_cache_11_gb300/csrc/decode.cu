@@ -40,19 +40,20 @@
 
 namespace pkv {
 
-template <int BS, int NCW, int NST>
+template <int BS, int NCW, int NST, int HT>
 struct DecodeSmem {
     static constexpr int kTileBytes = BS * kHeadDim * 2;  // one (block, KV head) tile of K or V
     static constexpr int kHalfBytes = kTileBytes / 2;     // its 64-column half
     static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
     static constexpr int kStagesBytes = NST * kStageBytes;
     static constexpr int kRedStride = kHeadDim + 4;       // floats per merged row
-    static constexpr int kRedBytes = NCW * kHeadTile * kRedStride * 4 + NCW * kHeadTile * 2 * 4;
-    static constexpr int kBarOffset = kStagesBytes;
+    static constexpr int kRedBytes = NCW * HT * kRedStride * 4 + NCW * HT * 2 * 4;
+    // the merge buffer reuses the ring once every stage has been consumed
+    static constexpr int kRingBytes = ((kStagesBytes > kRedBytes ? kStagesBytes : kRedBytes) + 1023) / 1024 * 1024;
+    static constexpr int kBarOffset = kRingBytes;
     static constexpr int kFlagOffset = kBarOffset + 2 * NST * 8;
     static constexpr int kTotal = kFlagOffset + 16;
     static constexpr int kDynamic = kTotal + 1024;        // slack to align the base to 1024 B
-    static_assert(kRedBytes <= kStagesBytes, "merge buffer must fit in the stage ring");
 };
 
 __device__ __forceinline__ void store_out(const DecodeParams& p, int s, int h, int d, float v) {
@@ -65,14 +66,33 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int s, int h, i
         static_cast<__half*>(p.out)[i] = __float2half_rn(v);
 }
 
-template <bool kBF16, int BS, int NCW, int NST>
-__global__ void __launch_bounds__((NCW + 1) * 32)
+// Tunables (compile-time): consumer warps per CTA, ring stages for 16- and
+// 32-token blocks, and the minimum resident CTAs per SM the register
+// allocation must allow.
+#ifndef PKV_NCW
+#define PKV_NCW 4
+#endif
+#ifndef PKV_NST16
+#define PKV_NST16 8
+#endif
+#ifndef PKV_NST32
+#define PKV_NST32 4
+#endif
+#ifndef PKV_MINB
+#define PKV_MINB 3
+#endif
+
+// NH: 8-head n-tiles per CTA (1: up to 8 query heads of a group, 2: up to 16).
+template <bool kBF16, int BS, int NH, int NCW, int NST>
+__global__ void __launch_bounds__((NCW + 1) * 32, PKV_MINB)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeParams p) {
-    using S = DecodeSmem<BS, NCW, NST>;
+    using S = DecodeSmem<BS, NCW, NST, 8 * NH>;
     constexpr int D = kHeadDim;
+    constexpr int HT = 8 * NH;     // query heads per CTA
     constexpr int kSub = BS / 16;  // 16-token sub-blocks per block
     static_assert(BS % 16 == 0, "block size must be a multiple of 16");
+    static_assert(NST % NCW == 0, "each ring stage must belong to one consumer warp");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_sa = smem_addr(smem_raw);
@@ -83,8 +103,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
     const int kvh = blockIdx.y / p.head_tiles;
     const int ht = blockIdx.y - kvh * p.head_tiles;
     const int s = blockIdx.z;
-    const int h0 = kvh * p.group + ht * kHeadTile;  // first query head of this CTA
-    const int rows = min(kHeadTile, p.group - ht * kHeadTile);
+    const int h0 = kvh * p.group + ht * HT;  // first query head of this CTA
+    const int rows = min(HT, p.group - ht * HT);
 
     const int L = __ldg(p.context_lens + s);
     const bool bad_len = L < 0 || L > p.len_limit;
@@ -119,11 +139,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
     }
     __syncthreads();
 
-    // consumer state (registers)
-    float o[16][4];
+    // Consumer state.  The contraction is written transposed: S^T = K Q^T with
+    // the 16 tokens of a sub-block as the MMA M dimension and the query heads
+    // as N (8 per n-tile), and O^T = V^T P^T with head_dim as M.  Thread
+    // (g = lane/4, t = lane%4) owns heads 8n + 2t, 8n + 2t + 1 of every tile.
+    float acc[8][NH][4];  // O^T: m-tile (16 dims) x n-tile x fragment
 #pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int n = 0; n < NH; ++n) acc[mt][n][0] = acc[mt][n][1] = acc[mt][n][2] = acc[mt][n][3] = 0.f;
+    float mrun[NH][2], lrun[NH][2];
+#pragma unroll
+    for (int n = 0; n < NH; ++n) mrun[n][0] = mrun[n][1] = -INFINITY, lrun[n][0] = lrun[n][1] = 0.f;
     int issued = 0;  // producer lane 0: TMA stages issued
 
     if (warp == NCW) {
@@ -174,25 +201,21 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
         }
     } else {
         // ------------------------------------------------------------ consumers
-        const int r0 = lane >> 2, r1 = r0 + 8, cq = 2 * (lane & 3);
-        // Q as the A operand of S = Q K^T: 8 k-steps of 16 dims.
-        uint32_t qa[8][4];
-        {
-            const uint32_t* q0 = r0 < rows ? reinterpret_cast<const uint32_t*>(
+        const int g = lane >> 2, t = lane & 3;
+        // Q^T as the B operand of S^T = K Q^T: for k-step ks, b0 holds
+        // q[head][16 ks + 2t .. +1], b1 holds q[head][16 ks + 8 + 2t .. +1].
+        uint32_t qb[NH][8][2];
+#pragma unroll
+        for (int n = 0; n < NH; ++n) {
+            const int hr = 8 * n + g;
+            const uint32_t* qr = hr < rows ? reinterpret_cast<const uint32_t*>(
                                                  static_cast<const uint16_t*>(p.q) +
-                                                 ((int64_t)s * p.num_q_heads + h0 + r0) * D)
-                                           : nullptr;
-            const uint32_t* q1 = r1 < rows ? reinterpret_cast<const uint32_t*>(
-                                                 static_cast<const uint16_t*>(p.q) +
-                                                 ((int64_t)s * p.num_q_heads + h0 + r1) * D)
+                                                 ((int64_t)s * p.num_q_heads + h0 + hr) * D)
                                            : nullptr;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const int c0 = (16 * ks + cq) >> 1, c1 = (16 * ks + 8 + cq) >> 1;
-                qa[ks][0] = q0 ? __ldg(q0 + c0) : 0u;
-                qa[ks][1] = q1 ? __ldg(q1 + c0) : 0u;
-                qa[ks][2] = q0 ? __ldg(q0 + c1) : 0u;
-                qa[ks][3] = q1 ? __ldg(q1 + c1) : 0u;
+                qb[n][ks][0] = qr ? __ldg(qr + 8 * ks + t) : 0u;
+                qb[n][ks][1] = qr ? __ldg(qr + 8 * ks + 4 + t) : 0u;
             }
         }
         const float sl2 = p.scale_log2;
@@ -216,116 +239,114 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
 #pragma unroll
             for (int sub = 0; sub < kSub; ++sub) {
                 if (sub * 16 >= valid) break;  // warp-uniform: nothing valid left in this block
-                // ---- S = Q K^T for tokens sub*16 .. sub*16+15
-                float sc[2][4];
+                // ---- S^T = K Q^T for tokens sub*16 .. sub*16+15 (M) x heads (N)
+                float sc[NH][4];
 #pragma unroll
-                for (int i = 0; i < 2; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+                for (int n = 0; n < NH; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
                 {
-                    // matrices: (tokens 0-7 | 8-15) x (dims lo | hi of the k-step)
-                    const int tok = sub * 16 + (mi >> 1) * 8 + rr;
+                    // A = K rows: matrices (tokens 0-7 | 8-15) x (dims lo | hi of the k-step)
+                    const int tok = sub * 16 + (mi & 1) * 8 + rr;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
-                        const int chunk = 2 * ks + (mi & 1);
+                        const int chunk = 2 * ks + (mi >> 1);
                         const int line = (chunk >> 3) * BS + tok;
                         const uint32_t addr = kb + line * 128 + (((chunk & 7) ^ rr) << 4);
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(addr, b0, b1, b2, b3);
-                        mma_16816<kBF16>(sc[0], qa[ks], b0, b1);
-                        mma_16816<kBF16>(sc[1], qa[ks], b2, b3);
+                        uint32_t a[4];
+                        ldsm_x4(addr, a[0], a[1], a[2], a[3]);
+#pragma unroll
+                        for (int n = 0; n < NH; ++n) mma_16816<kBF16>(sc[n], a, qb[n][ks][0], qb[n][ks][1]);
                     }
                 }
-                // ---- scale (log2 domain), mask past the context, online softmax
-                const int tb = sub * 16 + cq;  // token of sc[nt][0] is tb + 8 nt; sc[nt][1] is one more
-                float mx0 = -INFINITY, mx1 = -INFINITY;
+                // ---- scale (log2 domain), mask past the context, online softmax per head
+                const int ta = sub * 16 + g, tb = ta + 8;  // tokens of sc[.][0..1] and sc[.][2..3]
+                const bool va = ta < valid, vb_ = tb < valid;
+                uint32_t ph[NH][2], pl[NH][2];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int t = tb + 8 * nt;
-                    sc[nt][0] = t < valid ? sc[nt][0] * sl2 : -INFINITY;
-                    sc[nt][1] = t + 1 < valid ? sc[nt][1] * sl2 : -INFINITY;
-                    sc[nt][2] = t < valid ? sc[nt][2] * sl2 : -INFINITY;
-                    sc[nt][3] = t + 1 < valid ? sc[nt][3] * sl2 : -INFINITY;
-                    mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
-                    mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
-                }
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float al0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
-                const float al1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
-                const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
-                const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-                m0 = mn0;
-                m1 = mn1;
-                float pr[2][4];
+                for (int n = 0; n < NH; ++n) {
+                    sc[n][0] = va ? sc[n][0] * sl2 : -INFINITY;
+                    sc[n][1] = va ? sc[n][1] * sl2 : -INFINITY;
+                    sc[n][2] = vb_ ? sc[n][2] * sl2 : -INFINITY;
+                    sc[n][3] = vb_ ? sc[n][3] * sl2 : -INFINITY;
+                    float mx0 = fmaxf(sc[n][0], sc[n][2]), mx1 = fmaxf(sc[n][1], sc[n][3]);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    pr[nt][0] = exp2f(sc[nt][0] - ms0);
-                    pr[nt][1] = exp2f(sc[nt][1] - ms0);
-                    pr[nt][2] = exp2f(sc[nt][2] - ms1);
-                    pr[nt][3] = exp2f(sc[nt][3] - ms1);
-                }
-                l0 = l0 * al0 + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
-                l1 = l1 * al1 + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+                    for (int o = 4; o < 32; o <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                    }
+                    const float mn0 = fmaxf(mrun[n][0], mx0), mn1 = fmaxf(mrun[n][1], mx1);
+                    const float al0 = mn0 == -INFINITY ? 1.f : exp2f(mrun[n][0] - mn0);
+                    const float al1 = mn1 == -INFINITY ? 1.f : exp2f(mrun[n][1] - mn1);
+                    const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
+                    const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+                    mrun[n][0] = mn0;
+                    mrun[n][1] = mn1;
+                    const float p0 = exp2f(sc[n][0] - ms0), p1 = exp2f(sc[n][1] - ms1);
+                    const float p2 = exp2f(sc[n][2] - ms0), p3 = exp2f(sc[n][3] - ms1);
+                    lrun[n][0] = lrun[n][0] * al0 + (p0 + p2);
+                    lrun[n][1] = lrun[n][1] * al1 + (p1 + p3);
 #pragma unroll
-                for (int n2 = 0; n2 < 16; ++n2) {
-                    o[n2][0] *= al0;
-                    o[n2][1] *= al0;
-                    o[n2][2] *= al1;
-                    o[n2][3] *= al1;
+                    for (int mt = 0; mt < 8; ++mt) {
+                        acc[mt][n][0] *= al0;
+                        acc[mt][n][1] *= al1;
+                        acc[mt][n][2] *= al0;
+                        acc[mt][n][3] *= al1;
+                    }
+                    // P^T rows (tokens) x columns (heads) in the accumulator
+                    // layout; movmatrix.trans turns each 8x8 half into the B
+                    // operand layout of O^T = V^T P^T.  High part + residual.
+                    float r0, r1, r2, r3;
+                    const uint32_t h01 = pack2<kBF16>(p0, p1, r0, r1);
+                    const uint32_t h23 = pack2<kBF16>(p2, p3, r2, r3);
+                    const uint32_t l01 = pack2<kBF16>(p0 - r0, p1 - r1);
+                    const uint32_t l23 = pack2<kBF16>(p2 - r2, p3 - r3);
+                    ph[n][0] = movmatrix_trans(h01);
+                    ph[n][1] = movmatrix_trans(h23);
+                    pl[n][0] = movmatrix_trans(l01);
+                    pl[n][1] = movmatrix_trans(l23);
                 }
-                // ---- P as the A operand: high part + residual
-                uint32_t ph[4], pl[4];
+                // ---- O^T += V^T P^T over the 16 tokens
                 {
-                    float ra, rb;
-                    ph[0] = pack2<kBF16>(pr[0][0], pr[0][1], ra, rb);
-                    pl[0] = pack2<kBF16>(pr[0][0] - ra, pr[0][1] - rb);
-                    ph[1] = pack2<kBF16>(pr[0][2], pr[0][3], ra, rb);
-                    pl[1] = pack2<kBF16>(pr[0][2] - ra, pr[0][3] - rb);
-                    ph[2] = pack2<kBF16>(pr[1][0], pr[1][1], ra, rb);
-                    pl[2] = pack2<kBF16>(pr[1][0] - ra, pr[1][1] - rb);
-                    ph[3] = pack2<kBF16>(pr[1][2], pr[1][3], ra, rb);
-                    pl[3] = pack2<kBF16>(pr[1][2] - ra, pr[1][3] - rb);
-                }
-                // ---- O += P V over the 16 tokens
-                {
-                    // matrices: (tokens 0-7 | 8-15) x (8-column n-tiles 2qd | 2qd+1), transposed
-                    const int tok = sub * 16 + (mi & 1) * 8 + rr;
+                    // A = V^T: matrices (tokens 0-7 | 8-15) x (dims 16mt+0..7 | +8..15), transposed
+                    const int tok = sub * 16 + (mi >> 1) * 8 + rr;
                     const bool tail = sub * 16 + 16 > valid;
                     // V rows past the context may hold anything (even NaN): zero them
-                    // in the B fragments rather than rely on p == 0.
-                    const uint32_t keep0 = (tb < valid ? 0x0000ffffu : 0u) | (tb + 1 < valid ? 0xffff0000u : 0u);
+                    // in the A fragments rather than rely on p == 0.
+                    const int tt = sub * 16 + 2 * t;
+                    const uint32_t keep0 = (tt < valid ? 0x0000ffffu : 0u) | (tt + 1 < valid ? 0xffff0000u : 0u);
                     const uint32_t keep1 =
-                        (tb + 8 < valid ? 0x0000ffffu : 0u) | (tb + 9 < valid ? 0xffff0000u : 0u);
+                        (tt + 8 < valid ? 0x0000ffffu : 0u) | (tt + 9 < valid ? 0xffff0000u : 0u);
 #pragma unroll
-                    for (int qd = 0; qd < 8; ++qd) {
-                        const int chunk = 2 * qd + (mi >> 1);
+                    for (int mt = 0; mt < 8; ++mt) {
+                        const int chunk = 2 * mt + (mi & 1);
                         const int line = (chunk >> 3) * BS + tok;
                         const uint32_t addr = vb + line * 128 + (((chunk & 7) ^ rr) << 4);
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_trans(addr, b0, b1, b2, b3);
+                        uint32_t a[4];
+                        ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
                         if (tail) {
-                            b0 &= keep0;
-                            b1 &= keep1;
-                            b2 &= keep0;
-                            b3 &= keep1;
+                            a[0] &= keep0;
+                            a[1] &= keep0;
+                            a[2] &= keep1;
+                            a[3] &= keep1;
                         }
-                        mma_16816<kBF16>(o[2 * qd], ph, b0, b1);
-                        mma_16816<kBF16>(o[2 * qd], pl, b0, b1);
-                        mma_16816<kBF16>(o[2 * qd + 1], ph, b2, b3);
-                        mma_16816<kBF16>(o[2 * qd + 1], pl, b2, b3);
+#pragma unroll
+                        for (int n = 0; n < NH; ++n) {
+                            mma_16816<kBF16>(acc[mt][n], a, ph[n][0], ph[n][1]);
+                            mma_16816<kBF16>(acc[mt][n], a, pl[n][0], pl[n][1]);
+                        }
                     }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
         }
-        // full row sums: the four lanes of a quad hold disjoint token columns
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        // full per-head sums: the eight lanes g = 0..7 hold disjoint tokens
+#pragma unroll
+        for (int n = 0; n < NH; ++n)
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                lrun[n][0] += __shfl_xor_sync(0xffffffffu, lrun[n][0], o);
+                lrun[n][1] += __shfl_xor_sync(0xffffffffu, lrun[n][1], o);
+            }
     }
     __syncthreads();
 
@@ -341,26 +362,36 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
     __syncthreads();
 
     // ---- merge the per-warp states (stage memory is free now)
-    float* red = reinterpret_cast<float*>(smem);                // [NCW][16][kRedStride]
-    float* ml = red + NCW * kHeadTile * S::kRedStride;          // [NCW][16][2]
+    float* red = reinterpret_cast<float*>(smem);          // [NCW][HT][kRedStride]
+    float* ml = red + NCW * HT * S::kRedStride;            // [NCW][HT][2]
     if (warp < NCW) {
-        const int r0 = lane >> 2, r1 = r0 + 8, cq = 2 * (lane & 3);
-        if (r0 < rows) {
-            float* dst = red + (warp * kHeadTile + r0) * S::kRedStride + cq;
+        const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-            for (int n2 = 0; n2 < 16; ++n2) *reinterpret_cast<float2*>(dst + 8 * n2) = make_float2(o[n2][0], o[n2][1]);
-            if ((lane & 3) == 0) {
-                ml[(warp * kHeadTile + r0) * 2] = m0;
-                ml[(warp * kHeadTile + r0) * 2 + 1] = l0;
+        for (int n = 0; n < NH; ++n) {
+            const int ha = 8 * n + 2 * t, hb = ha + 1;
+            float* ra = red + (warp * HT + ha) * S::kRedStride;
+            float* rb = red + (warp * HT + hb) * S::kRedStride;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const int d0 = 16 * mt + g;
+                if (ha < rows) {
+                    ra[d0] = acc[mt][n][0];
+                    ra[d0 + 8] = acc[mt][n][2];
+                }
+                if (hb < rows) {
+                    rb[d0] = acc[mt][n][1];
+                    rb[d0 + 8] = acc[mt][n][3];
+                }
             }
-        }
-        if (r1 < rows) {
-            float* dst = red + (warp * kHeadTile + r1) * S::kRedStride + cq;
-#pragma unroll
-            for (int n2 = 0; n2 < 16; ++n2) *reinterpret_cast<float2*>(dst + 8 * n2) = make_float2(o[n2][2], o[n2][3]);
-            if ((lane & 3) == 0) {
-                ml[(warp * kHeadTile + r1) * 2] = m1;
-                ml[(warp * kHeadTile + r1) * 2 + 1] = l1;
+            if (g == 0) {
+                if (ha < rows) {
+                    ml[(warp * HT + ha) * 2] = mrun[n][0];
+                    ml[(warp * HT + ha) * 2 + 1] = lrun[n][0];
+                }
+                if (hb < rows) {
+                    ml[(warp * HT + hb) * 2] = mrun[n][1];
+                    ml[(warp * HT + hb) * 2 + 1] = lrun[n][1];
+                }
             }
         }
     }
@@ -368,28 +399,28 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
 
     const bool bad = fl != 0;
     for (int i = tid; i < rows * D; i += blockDim.x) {
-        const int g = i / D, d = i % D;
+        const int hr = i / D, d = i % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NCW; ++w) M = fmaxf(M, ml[(w * kHeadTile + g) * 2]);
-        float lsum = 0.f, acc = 0.f;
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, ml[(w * HT + hr) * 2]);
+        float lsum = 0.f, o = 0.f;
 #pragma unroll
         for (int w = 0; w < NCW; ++w) {
-            const float mw = ml[(w * kHeadTile + g) * 2];
+            const float mw = ml[(w * HT + hr) * 2];
             if (mw != -INFINITY) {
                 const float f = exp2f(mw - M);
-                lsum += f * ml[(w * kHeadTile + g) * 2 + 1];
-                acc += f * red[(w * kHeadTile + g) * S::kRedStride + d];
+                lsum += f * ml[(w * HT + hr) * 2 + 1];
+                o += f * red[(w * HT + hr) * S::kRedStride + d];
             }
         }
-        const int h = h0 + g;
+        const int h = h0 + hr;
         if (write_partial) {
             const int64_t idx = ((int64_t)s * p.num_q_heads + h) * p.max_parts + part;
-            p.part_o[idx * D + d] = bad ? 0.f : acc / lsum;
+            p.part_o[idx * D + d] = bad ? 0.f : o / lsum;
             // +inf marks a partition whose metadata was bad: the merge zeroes the output.
             if (d == 0) p.part_lse[idx] = bad ? INFINITY : M + log2f(lsum);
         } else {
-            store_out(p, s, h, d, bad ? 0.f : acc / lsum);
+            store_out(p, s, h, d, bad ? 0.f : o / lsum);
         }
     }
 }
@@ -425,11 +456,13 @@ __global__ void __launch_bounds__(kHeadDim) reduce_kernel(const DecodeParams p) 
     store_out(p, s, h, d, bad ? 0.f : acc / sum);
 }
 
-template <bool kBF16, int BS, int NCW, int NST>
+template <bool kBF16, int BS, int NH>
 static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
                                    cudaStream_t stream, int* launches) {
-    using S = DecodeSmem<BS, NCW, NST>;
-    auto kern = decode_kernel<kBF16, BS, NCW, NST>;
+    constexpr int NCW = PKV_NCW;
+    constexpr int NST = BS == 16 ? PKV_NST16 : PKV_NST32;
+    using S = DecodeSmem<BS, NCW, NST, 8 * NH>;
+    auto kern = decode_kernel<kBF16, BS, NH, NCW, NST>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kDynamic);
     if (e != cudaSuccess) return e;
     const dim3 grid(p.max_parts, p.num_kv_heads * p.head_tiles, p.num_seqs);
@@ -446,14 +479,22 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmk
     return cudaSuccess;
 }
 
+int decode_head_tile(int group) { return group <= 8 ? 8 : 16; }
+
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int block_size, const CUtensorMap& tmk,
                           const CUtensorMap& tmv, cudaStream_t stream, int* launches) {
     const bool bf16 = dtype == PKV_BF16;
-    if (block_size == 16)
-        return bf16 ? launch_decode_t<true, 16, 4, 8>(p, tmk, tmv, stream, launches)
-                    : launch_decode_t<false, 16, 4, 8>(p, tmk, tmv, stream, launches);
-    return bf16 ? launch_decode_t<true, 32, 4, 4>(p, tmk, tmv, stream, launches)
-                : launch_decode_t<false, 32, 4, 4>(p, tmk, tmv, stream, launches);
+    const bool wide = decode_head_tile(p.group) == 16;
+#define PKV_DISPATCH(BS_)                                                                              \
+    return bf16 ? (wide ? launch_decode_t<true, BS_, 2>(p, tmk, tmv, stream, launches)                 \
+                        : launch_decode_t<true, BS_, 1>(p, tmk, tmv, stream, launches))                \
+                : (wide ? launch_decode_t<false, BS_, 2>(p, tmk, tmv, stream, launches)                \
+                        : launch_decode_t<false, BS_, 1>(p, tmk, tmv, stream, launches));
+    if (block_size == 16) {
+        PKV_DISPATCH(16)
+    }
+    PKV_DISPATCH(32)
+#undef PKV_DISPATCH
 }
 
 }  // namespace pkv

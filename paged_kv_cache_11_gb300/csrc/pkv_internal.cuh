@@ -16,7 +16,6 @@ namespace pkv {
 
 constexpr int kHeadDim = 128;          // supported head_dim
 constexpr int kAutoPartition = 512;    // tokens per split-K partition when the caller passes 0
-constexpr int kHeadTile = 16;          // query heads of one GQA group handled by one CTA (mma M)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on any in-CTA wait (2 s)
 
 // The per-device error word lives in the API translation unit; kernels get
@@ -41,11 +40,14 @@ struct DecodeParams {
     int partition_size;          // tokens, multiple of block_size
     int max_parts;               // ceil(max_context_len / partition_size), >= 1
     int group;                   // G = Hq / Hkv
-    int head_tiles;              // ceil(G / kHeadTile)
+    int head_tiles;              // ceil(G / decode_head_tile(G))
     int out_dtype;               // pkv_dtype
     int split;                   // 1: sequences with > 1 partition write partials
     float scale_log2;            // scale * log2(e)
 };
+
+// Query heads of one GQA group handled by one decode CTA (8 or 16).
+int decode_head_tile(int group);
 
 // Host-side launchers (decode.cu); return a cudaError_t from the launch.
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int block_size, const CUtensorMap& tmk,
@@ -205,4 +207,14 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return pack2<kBF16>(lo, hi, a, b);
 }
 
+}  // namespace pkv
+
+namespace pkv {
+// Transpose an 8x8 matrix of 16-bit elements held in the standard warp
+// fragment layout (thread l: row l/4, columns 2(l%4), 2(l%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
 }  // namespace pkv
