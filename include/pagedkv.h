@@ -113,9 +113,19 @@ pkv_status paged_kv_append(const void* k, const void* v, const int64_t* slot_map
 /*
  * Bytes of workspace paged_attention_decode needs for these sizes (0 when
  * the call runs in a single pass).  partition_size as for
- * paged_attention_decode (0 = automatic).  Returns 0 for invalid sizes.
+ * paged_attention_decode; with 0 (automatic) the size covers the smallest
+ * automatic partition, so it is enough whatever the call picks.  Returns 0
+ * for invalid sizes.
  */
 size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                       int32_t max_context_len, int32_t partition_size);
+
+/*
+ * The split-K partition size (tokens) paged_attention_decode uses for these
+ * sizes on the current device: partition_size itself when it is non-zero,
+ * else the automatic choice.  Returns 0 for invalid sizes.
+ */
+int32_t paged_attention_partition_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t max_context_len, int32_t partition_size);
 
 /*
@@ -140,8 +150,9 @@ size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, in
  * out:             [num_seqs][num_q_heads][head_dim] of out_dtype (PKV_FP32,
  *                  PKV_BF16 or PKV_FP16), 16-byte aligned.
  * partition_size:  tokens per split-K partition, a multiple of block_size;
- *                  0 picks 512.  When max_context_len > partition_size each
- *                  partition writes (o_p, lse_p) to the workspace and a
+ *                  0 picks 512, 1024 or 2048 from the amount of work and the
+ *                  device's SM count.  When max_context_len > partition_size
+ *                  each partition writes (o_p, lse_p) to the workspace and a
  *                  second kernel merges them through their log-sum-exp;
  *                  otherwise one kernel writes out directly.
  * workspace:       device memory of at least

@@ -63,6 +63,8 @@ def _lib() -> ctypes.CDLL:
     lib.paged_kv_append.restype = ctypes.c_int
     lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.paged_attention_workspace_bytes.restype = sz
+    lib.paged_attention_partition_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.paged_attention_partition_size.restype = i32
     lib.paged_attention_decode.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp, i32,
                                            desc_p, i32, vp, sz, vp]
     lib.paged_attention_decode.restype = ctypes.c_int
@@ -132,6 +134,13 @@ def paged_attention_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: i
                                     partition_size: int = 0) -> int:
     return int(_lib().paged_attention_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
                                                       partition_size))
+
+
+def paged_attention_partition_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, max_context_len: int,
+                                   partition_size: int = 0) -> int:
+    """Split-K partition (tokens) a decode call with these sizes uses on the current device."""
+    return int(_lib().paged_attention_partition_size(num_seqs, num_q_heads, num_kv_heads, max_context_len,
+                                                     partition_size))
 
 
 def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

@@ -77,7 +77,35 @@ static pkv_status check_cache(const pkv_cache_desc* c) {
     return PKV_OK;
 }
 
-static int resolve_partition(int32_t partition_size) { return partition_size == 0 ? kAutoPartition : partition_size; }
+// Streaming multiprocessors of the current device (cached per device).
+static int sm_count() {
+    static int cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Tokens per split-K partition.  An explicit size is used as given.  The
+// automatic choice takes the largest of 512, 1024, 2048 tokens for which the
+// work units (sequence x KV head x head tile x partition, counted at
+// max_context_len) still fill the GPU's resident decode CTAs at least twice;
+// longer partitions amortise each CTA's start-up, shorter ones balance the
+// load.  The workspace is always sized for 512 (the smallest choice).
+static int resolve_partition(int32_t partition_size, int64_t rows, int32_t max_context_len) {
+    if (partition_size != 0) return partition_size;
+    const int64_t slots = (int64_t)(sm_count() > 0 ? sm_count() : 148) * kDecodeCtasPerSm;
+    int best = kAutoPartition;
+    for (int P = 1024; P <= 2048; P *= 2) {
+        const int64_t units = rows * (((int64_t)max_context_len + P - 1) / P);
+        if (units >= 2 * slots) best = P;
+    }
+    return best;
+}
 
 }  // namespace pkv
 
@@ -138,13 +166,23 @@ pkv_status paged_kv_append(const void* k, const void* v, const int64_t* slot_map
 size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                        int32_t max_context_len, int32_t partition_size) {
     if (num_seqs < 0 || num_q_heads < 1 || head_dim < 1 || max_context_len < 0 || partition_size < 0) return 0;
-    const int64_t P = resolve_partition(partition_size);
+    const int64_t P = partition_size == 0 ? kAutoPartition : partition_size;  // auto never goes below 512
     const int64_t parts = max_context_len == 0 ? 1 : (max_context_len + P - 1) / P;
     if (parts <= 1) return 0;
     const int64_t rows = (int64_t)num_seqs * num_q_heads * parts;
     const int64_t o_bytes = ((rows * head_dim * 4) + 255) / 256 * 256;
     const int64_t lse_bytes = ((rows * 4) + 255) / 256 * 256;
     return (size_t)(o_bytes + lse_bytes);
+}
+
+int32_t paged_attention_partition_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t max_context_len, int32_t partition_size) {
+    if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 ||
+        max_context_len < 0 || partition_size < 0)
+        return 0;
+    const int group = num_q_heads / num_kv_heads;
+    const int head_tiles = (group + decode_head_tile(group) - 1) / decode_head_tile(group);
+    return resolve_partition(partition_size, (int64_t)num_seqs * num_kv_heads * head_tiles, max_context_len);
 }
 
 pkv_status paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -178,7 +216,8 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
         !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return PKV_ERR_INVALID_ARG;
 
-    const int P = resolve_partition(partition_size);
+    const int P = resolve_partition(partition_size, (int64_t)num_seqs * cache->num_kv_heads * head_tiles,
+                                    max_context_len);
     const int max_parts = max_context_len == 0 ? 1 : (max_context_len + P - 1) / P;
     const bool split = max_parts > 1;
     const size_t need = paged_attention_workspace_bytes(num_seqs, num_q_heads, kHeadDim, max_context_len,

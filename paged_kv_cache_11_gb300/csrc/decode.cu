@@ -70,16 +70,16 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int s, int h, i
 // 32-token blocks, and the minimum resident CTAs per SM the register
 // allocation must allow.
 #ifndef PKV_NCW
-#define PKV_NCW 4
+#define PKV_NCW 2
 #endif
 #ifndef PKV_NST16
-#define PKV_NST16 8
+#define PKV_NST16 4
 #endif
 #ifndef PKV_NST32
-#define PKV_NST32 4
+#define PKV_NST32 2
 #endif
 #ifndef PKV_MINB
-#define PKV_MINB 3
+#define PKV_MINB kDecodeCtasPerSm
 #endif
 
 // NH: 8-head n-tiles per CTA (1: up to 8 query heads of a group, 2: up to 16).

@@ -15,7 +15,8 @@
 namespace pkv {
 
 constexpr int kHeadDim = 128;          // supported head_dim
-constexpr int kAutoPartition = 512;    // tokens per split-K partition when the caller passes 0
+constexpr int kAutoPartition = 512;    // smallest automatic split-K partition (tokens)
+constexpr int kDecodeCtasPerSm = 5;    // resident decode CTAs per SM the kernel is tuned for
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on any in-CTA wait (2 s)
 
 // The per-device error word lives in the API translation unit; kernels get

@@ -26,7 +26,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = set(declared_functions())
     assert {"paged_kv_append", "paged_attention_decode", "copy_blocks", "paged_attention_workspace_bytes",
-            "pkv_check_device_error", "pkv_status_string", "pkv_launch_count", "pkv_version"} <= names
+            "pkv_check_device_error", "pkv_status_string", "pkv_launch_count", "pkv_version",
+            "paged_attention_partition_size"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -71,6 +72,12 @@ def test_decode_host_validation(lib):
     assert _decode(lib, d, ptr=18) == binding.PKV_ERR_INVALID_ARG             # misaligned pointers
     assert _decode(lib, d, max_ctx=64, P=16) == binding.PKV_ERR_WORKSPACE     # split needs a workspace
     assert _decode(lib, d, num_seqs=70000) == binding.PKV_ERR_INVALID_ARG
+
+
+def test_partition_size_query(lib):
+    assert binding.paged_attention_partition_size(8, 64, 8, 131072, 256) == 256   # explicit: as given
+    assert binding.paged_attention_partition_size(8, 64, 7, 131072, 0) == 0       # 64 % 7 != 0
+    assert binding.paged_attention_partition_size(8, 64, 8, 131072, 0) in (512, 1024, 2048)
 
 
 def test_workspace_bytes(lib):

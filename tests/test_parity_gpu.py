@@ -139,7 +139,7 @@ def test_split_k_matches_single_pass(gpu):
 
 def test_shared_blocks_equal_copied_blocks(gpu):
     """Sequences mapping the group's shared prefix == the same sequences with private copies."""
-    wl = W.make_workload("shared_prefix", groups=1, per_group=3, prefix=64, suffix=(32, 60))
+    wl = W.make_workload("shared_prefix", groups=1, per_group=3, prefix=64, suffix=(32, 60), pool_blocks=64)
     _, _, shared = gpu_step(wl, gpu)
     # give sequences 1 and 2 private copies of the 4 shared prefix blocks
     free = sorted(set(range(wl.num_blocks)) - set(wl.block_tables[wl.block_tables >= 0].tolist()))
