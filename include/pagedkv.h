@@ -172,6 +172,32 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
                                   size_t workspace_bytes, void* stream);
 
 /*
+ * paged_attention_decode without a workspace argument, for callers that
+ * cannot allocate device memory: a process whose device memory is all owned
+ * by another allocator (such as a serving engine that reserved nearly all of
+ * HBM for its KV pool at start-up), or a latency-critical loop that must not
+ * call cudaMalloc because it can implicitly synchronise the device.  The
+ * pages have no counterpart to this call; it is an addition of this library.
+ *
+ * Arguments and results are those of paged_attention_decode.  The split-K
+ * partials live in a file-scope device array of 16 MiB that every GPU which
+ * loads the library holds until the process exits; a call whose
+ * paged_attention_workspace_bytes(...) exceeds 16 MiB is rejected with
+ * PKV_ERR_WORKSPACE before anything is launched.  The call allocates nothing.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  The array is shared by every call on the
+ * device and keeps the last call's contents; nothing in it needs to start at
+ * zero.  Calls whose kernels overlap on the GPU race on the array: the caller
+ * must serialise them.
+ */
+pkv_status paged_attention_decode_static(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_context_len, float scale, void* out, int32_t out_dtype,
+                                         const pkv_cache_desc* cache, int32_t partition_size, void* stream);
+
+/*
  * Batched copy-on-write block copy ("vllm", "como funciona": a write into
  * the last shared block copies that block and only it; "o que isso
  * custou": batched block copy).

@@ -68,6 +68,9 @@ def _lib() -> ctypes.CDLL:
     lib.paged_attention_decode.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp, i32,
                                            desc_p, i32, vp, sz, vp]
     lib.paged_attention_decode.restype = ctypes.c_int
+    lib.paged_attention_decode_static.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp,
+                                                  i32, desc_p, i32, vp]
+    lib.paged_attention_decode_static.restype = ctypes.c_int
     lib.copy_blocks.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, i32, desc_p, vp]
     lib.copy_blocks.restype = ctypes.c_int
     lib.pkv_check_device_error.argtypes = [vp, ctypes.POINTER(i32)]
@@ -175,6 +178,24 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), num_seqs, hq,
         int(max_context_len), float(scale), _ptr(out), _DTYPE_CODE.get(out.dtype, -1), ctypes.byref(desc),
         int(partition_size), _ptr(workspace), ws_bytes, _stream(stream)), "paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_static(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                  block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                                  out: torch.Tensor, max_context_len: int, partition_size: int = 0,
+                                  stream=None) -> torch.Tensor:
+    """paged_attention_decode for callers that cannot allocate device memory: no
+    workspace argument, the split-K partials go to the library's fixed 16 MiB
+    device array (calls needing more raise PagedKVError(PKV_ERR_WORKSPACE))."""
+    for t in (q, k_cache, v_cache, block_tables, context_lens, out):
+        _require(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    desc = cache_desc(k_cache)
+    num_seqs, hq, _ = q.shape
+    _check(_lib().paged_attention_decode_static(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+        num_seqs, hq, int(max_context_len), float(scale), _ptr(out), _DTYPE_CODE.get(out.dtype, -1),
+        ctypes.byref(desc), int(partition_size), _stream(stream)), "paged_attention_decode_static")
     return out
 
 
