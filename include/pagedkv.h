@@ -72,8 +72,8 @@ typedef enum { PKV_BF16 = 0, PKV_FP16 = 1, PKV_FP32 = 2 } pkv_dtype;
 /* Codes stored in the device error word (first error wins). */
 enum {
     PKV_DEVERR_NONE = 0,
-    PKV_DEVERR_SLOT = 1,        /* append: slot >= num_blocks * block_size */
-    PKV_DEVERR_COPY_ID = 2,     /* copy_blocks: src or dst outside the pool */
+    PKV_DEVERR_SLOT = 1,        /* append / compact_tokens: slot >= num_blocks * block_size */
+    PKV_DEVERR_COPY_ID = 2,     /* copy_blocks / swap_blocks: src or dst outside its pool */
     PKV_DEVERR_CONTEXT_LEN = 3, /* decode: context_lens[s] < 0, above the table's capacity, or above max_context_len */
     PKV_DEVERR_BLOCK_ID = 4,    /* decode: block_tables entry outside the pool */
     PKV_DEVERR_TIMEOUT = 5      /* a bounded in-CTA wait ran out */
@@ -152,13 +152,18 @@ int32_t paged_attention_partition_size(int32_t num_seqs, int32_t num_q_heads, in
  * partition_size:  tokens per split-K partition, a multiple of block_size;
  *                  0 picks 512, 1024 or 2048 from the amount of work and the
  *                  device's SM count.  When max_context_len > partition_size
- *                  each partition writes (o_p, lse_p) to the workspace and a
- *                  second kernel merges them through their log-sum-exp;
- *                  otherwise one kernel writes out directly.
+ *                  each partition writes (o_p, lse_p) to the workspace and
+ *                  they are merged through their log-sum-exp: by the last
+ *                  partition of each (sequence, head group) to finish when a
+ *                  sequence has at most 16 partitions, else by a second
+ *                  kernel.  Otherwise one kernel writes out directly.
  * workspace:       device memory of at least
  *                  paged_attention_workspace_bytes(...) bytes, 256-byte
  *                  aligned (may be NULL when that is 0).  Contents on entry
- *                  are ignored.
+ *                  are ignored: the merge's arrival counters carry the
+ *                  epoch of the call that wrote them, and a counter of any
+ *                  other epoch counts as zero.  Two calls whose kernels may
+ *                  overlap on the GPU must not share a workspace.
  * Supported: head_dim 128; block_size 16 or 32; bf16 or fp16 caches;
  * num_q_heads a multiple of num_kv_heads; num_seqs <= 65535.
  * Results depend only on logical token order: permuting physical block ids
@@ -170,6 +175,31 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
                                   int32_t max_context_len, float scale, void* out, int32_t out_dtype,
                                   const pkv_cache_desc* cache, int32_t partition_size, void* workspace,
                                   size_t workspace_bytes, void* stream);
+
+/*
+ * A decode step in one launch: the block write of one new token per
+ * sequence ("vllm", "o que isso custou": block write) fused into
+ * paged_attention_decode.  The result, and the cache afterwards, are those
+ * of paged_kv_append(k_new, v_new, slot_mapping, num_seqs, ...) followed by
+ * paged_attention_decode(...), provided that each sequence's new token is its
+ * last context position: slot_mapping[s] must be the slot of position
+ * context_lens[s] - 1 of sequence s (block_tables[s][(L-1)/bs] * bs +
+ * (L-1) % bs), or negative when sequence s has no new token, and no other
+ * sequence may read that slot in this call.  A slot that is not that position
+ * is not written and is recorded as PKV_DEVERR_SLOT.
+ * k_new, v_new:  [num_seqs][num_kv_heads][head_dim], cache dtype, 16-byte
+ *                aligned device memory.
+ * slot_mapping:  [num_seqs] int64 device memory.
+ * Other arguments as for paged_attention_decode; k_cache and v_cache are
+ * written.
+ */
+pkv_status paged_attention_append_decode(const void* q, const void* k_new, const void* v_new,
+                                         const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_context_len, float scale, void* out, int32_t out_dtype,
+                                         const pkv_cache_desc* cache, int32_t partition_size, void* workspace,
+                                         size_t workspace_bytes, void* stream);
 
 /*
  * paged_attention_decode without a workspace argument, for callers that
@@ -215,6 +245,45 @@ pkv_status paged_attention_decode_static(const void* q, const void* k_cache, con
 pkv_status copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
                        const int64_t* src_dst_pairs, int32_t num_pairs, const pkv_cache_desc* cache,
                        void* stream);
+
+/*
+ * Swap-out / swap-in of whole blocks between two pools ("vllm", "como
+ * funciona": a preempted sequence's blocks go to CPU RAM and come back).
+ * For each pair i and each layer l:
+ *     dst_k_caches[l][dst] = src_k_caches[l][src]   (and the V caches)
+ * with (src, dst) = (src_dst_pairs[2i], src_dst_pairs[2i+1]), src a block of
+ * the source pool (src_num_blocks blocks) and dst one of the destination
+ * pool (dst_num_blocks blocks).  Either pool may be GPU memory or page-locked
+ * host memory that the GPU addresses directly (cudaHostAlloc, or
+ * cudaHostRegister'ed memory, on a unified-addressing system; on GB300 the
+ * copy runs over NVLink-C2C).  Both pools have the per-block shape of
+ * `cache` (its num_blocks is not used).
+ * src_k_caches, ...: HOST arrays of num_layers pointers, 16-byte aligned.
+ * src_dst_pairs:    [num_pairs][2] int64, GPU-addressable memory.
+ * An id outside its pool skips that pair and records PKV_DEVERR_COPY_ID.
+ * Destinations must be distinct.  Bit-exact.
+ */
+pkv_status swap_blocks(void* const* src_k_caches, void* const* src_v_caches, int64_t src_num_blocks,
+                       void* const* dst_k_caches, void* const* dst_v_caches, int64_t dst_num_blocks,
+                       int32_t num_layers, const int64_t* src_dst_pairs, int32_t num_pairs,
+                       const pkv_cache_desc* cache, void* stream);
+
+/*
+ * Token-level compaction into fresh target blocks (gist.science "Zipage",
+ * Compressed PagedAttention: once a request holds N_max blocks and the last
+ * one is full, the tokens it keeps are rewritten into new target blocks --
+ * the first N_max - 1 of its new table -- so that prefix blocks shared with
+ * other requests stay intact).  For each i with both slots >= 0:
+ *     k_cache[dst slot row of head h] = k_cache[src slot row of head h]
+ * for every KV head h, and the same for v_cache.  The caller chooses the
+ * kept tokens (their scoring is not part of this library) and the target
+ * blocks.  No destination slot may also be a source slot, and destinations
+ * must be distinct.  A slot >= num_blocks * block_size skips the token and
+ * records PKV_DEVERR_SLOT.  src_slots, dst_slots: [num_tokens] int64 device
+ * memory.  Bit-exact.
+ */
+pkv_status compact_tokens(const int64_t* src_slots, const int64_t* dst_slots, int64_t num_tokens, void* k_cache,
+                          void* v_cache, const pkv_cache_desc* cache, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error

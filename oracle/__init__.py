@@ -10,6 +10,8 @@ Functions (sources cited in ``pkv_oracle.c``):
 
 * ``append``      -- block write of new K/V rows into their slots
 * ``copy_blocks`` -- whole-block copy of (src, dst) pairs
+* ``swap_blocks`` -- whole-block moves between two pools (swap out / in)
+* ``compact``     -- token-row moves into fresh target blocks (Zipage)
 * ``decode``      -- softmax(scale * q . K) V over each sequence's context,
                      gathered through its block table; optional partitioned
                      (split-K) form and optional subset of (seq, head) outputs
@@ -61,6 +63,10 @@ def _lib():
         lib.oracle_append.restype = i64
         lib.oracle_copy_blocks.argtypes = [vp, vp, vp, i64, i64, i32, i32, i32]
         lib.oracle_copy_blocks.restype = i64
+        lib.oracle_swap_blocks.argtypes = [vp, vp, i64, vp, vp, i64, vp, i64, i32, i32, i32]
+        lib.oracle_swap_blocks.restype = i64
+        lib.oracle_compact.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i32]
+        lib.oracle_compact.restype = i64
         lib.oracle_decode.argtypes = [i32, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, ctypes.c_double,
                                       i32, vp, vp, i64, vp, i32]
         lib.oracle_decode.restype = i64
@@ -95,6 +101,25 @@ def copy_blocks(k_cache, v_cache, pairs) -> int:
     pr = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
     nb, hkv, bs, d = kc.shape
     return int(_lib().oracle_copy_blocks(kc.ctypes.data, vc.ctypes.data, pr.ctypes.data, pr.shape[0], nb, hkv, bs, d))
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, pairs) -> int:
+    """Whole blocks src (of the source pool) -> dst (of the destination pool), in place on dst."""
+    sk, sv, dk, dv = (_u16(a, n) for a, n in ((src_k, "src_k"), (src_v, "src_v"), (dst_k, "dst_k"), (dst_v, "dst_v")))
+    pr = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    _, hkv, bs, d = sk.shape
+    return int(_lib().oracle_swap_blocks(sk.ctypes.data, sv.ctypes.data, sk.shape[0], dk.ctypes.data, dv.ctypes.data,
+                                         dk.shape[0], pr.ctypes.data, pr.shape[0], hkv, bs, d))
+
+
+def compact(k_cache, v_cache, src_slots, dst_slots) -> int:
+    """Token rows src slot -> dst slot (every head, K and V), in place."""
+    kc, vc = _u16(k_cache, "k_cache"), _u16(v_cache, "v_cache")
+    a = np.ascontiguousarray(src_slots, dtype=np.int64)
+    b = np.ascontiguousarray(dst_slots, dtype=np.int64)
+    nb, hkv, bs, d = kc.shape
+    return int(_lib().oracle_compact(kc.ctypes.data, vc.ctypes.data, a.ctypes.data, b.ctypes.data, a.size, nb, hkv,
+                                     bs, d))
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, dtype: str, partition_size: int = 0,

@@ -22,6 +22,12 @@
  *   [aitalk] aitalk.it "PagedAttention e RadixAttention", section
  *            "PagedAttention: la memoria come un sistema operativo" (the
  *            same four steps; outputs unchanged).
+ *   [Zipage] gist.science summary of "Zipage: Maintain High Request
+ *            Concurrency for LLM Reasoning through Compressed
+ *            PagedAttention", technical summary, section 2 (a request holds
+ *            at most N_max blocks; kept tokens are rewritten into new target
+ *            blocks, the first N_max - 1 of them, leaving shared blocks
+ *            intact).
  *
  * Readings where the pages leave a point open (each also listed in the
  * design notes):
@@ -136,6 +142,56 @@ int64_t oracle_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, const int64_t* 
         }
         memcpy(k_cache + dst * blk, k_cache + src * blk, sizeof(uint16_t) * (size_t)blk);
         memcpy(v_cache + dst * blk, v_cache + src * blk, sizeof(uint16_t) * (size_t)blk);
+    }
+    return bad;
+}
+
+/*
+ * Swap of whole blocks between two pools [vLLM "como funciona": the blocks
+ * of an evicted sequence go to CPU RAM and are brought back]: block src of
+ * the source pool becomes block dst of the destination pool, every KV head
+ * and slot, K and V.  Returns the number of pairs with an id outside its
+ * pool (skipped).
+ */
+int64_t oracle_swap_blocks(const uint16_t* src_k, const uint16_t* src_v, int64_t src_num_blocks, uint16_t* dst_k,
+                           uint16_t* dst_v, int64_t dst_num_blocks, const int64_t* pairs, int64_t num_pairs,
+                           int num_kv_heads, int block_size, int head_dim) {
+    int64_t bad = 0;
+    int64_t blk = (int64_t)num_kv_heads * block_size * head_dim;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
+            ++bad;
+            continue;
+        }
+        memcpy(dst_k + dst * blk, src_k + src * blk, sizeof(uint16_t) * (size_t)blk);
+        memcpy(dst_v + dst * blk, src_v + src * blk, sizeof(uint16_t) * (size_t)blk);
+    }
+    return bad;
+}
+
+/*
+ * Token-level compaction [Zipage, Compressed PagedAttention: the kept tokens
+ * of a request are rewritten into new target blocks]: the K and V rows of
+ * every KV head move from slot src_slots[i] to slot dst_slots[i].  Negative
+ * slots are skipped; slots outside the pool are counted and skipped.
+ */
+int64_t oracle_compact(uint16_t* k_cache, uint16_t* v_cache, const int64_t* src_slots, const int64_t* dst_slots,
+                       int64_t num_tokens, int64_t num_blocks, int num_kv_heads, int block_size, int head_dim) {
+    int64_t bad = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t a = src_slots[t], b = dst_slots[t];
+        if (a < 0 || b < 0) continue;
+        if (a >= num_blocks * block_size || b >= num_blocks * block_size) {
+            ++bad;
+            continue;
+        }
+        for (int h = 0; h < num_kv_heads; ++h) {
+            int64_t from = (((a / block_size) * num_kv_heads + h) * block_size + a % block_size) * head_dim;
+            int64_t to = (((b / block_size) * num_kv_heads + h) * block_size + b % block_size) * head_dim;
+            memcpy(k_cache + to, k_cache + from, sizeof(uint16_t) * (size_t)head_dim);
+            memcpy(v_cache + to, v_cache + from, sizeof(uint16_t) * (size_t)head_dim);
+        }
     }
     return bad;
 }

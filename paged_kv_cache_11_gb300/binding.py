@@ -68,11 +68,19 @@ def _lib() -> ctypes.CDLL:
     lib.paged_attention_decode.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp, i32,
                                            desc_p, i32, vp, sz, vp]
     lib.paged_attention_decode.restype = ctypes.c_int
+    lib.paged_attention_append_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                                  ctypes.c_float, vp, i32, desc_p, i32, vp, sz, vp]
+    lib.paged_attention_append_decode.restype = ctypes.c_int
     lib.paged_attention_decode_static.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp,
                                                   i32, desc_p, i32, vp]
     lib.paged_attention_decode_static.restype = ctypes.c_int
     lib.copy_blocks.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, i32, desc_p, vp]
     lib.copy_blocks.restype = ctypes.c_int
+    lib.swap_blocks.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i64, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                i64, i32, vp, i32, desc_p, vp]
+    lib.swap_blocks.restype = ctypes.c_int
+    lib.compact_tokens.argtypes = [vp, vp, i64, vp, vp, desc_p, vp]
+    lib.compact_tokens.restype = ctypes.c_int
     lib.pkv_check_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     lib.pkv_check_device_error.restype = ctypes.c_int
     _LIB = lib
@@ -181,6 +189,37 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     return out
 
 
+def paged_attention_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                  slot_mapping: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                  block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                                  out: torch.Tensor | None = None, max_context_len: int | None = None,
+                                  partition_size: int = 0, workspace: torch.Tensor | None = None,
+                                  out_dtype: torch.dtype = torch.float32, stream=None) -> torch.Tensor:
+    """One decode step in one launch: write sequence s's new token (k_new[s], v_new[s]) to
+    slot_mapping[s] -- the slot of its last context position -- then attend."""
+    for t in (q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, context_lens):
+        _require(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == q.shape[0],
+             "slot_mapping: int64, one slot per sequence")
+    desc = cache_desc(k_cache)
+    num_seqs, hq, d = q.shape
+    max_blocks = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = max_blocks * desc.block_size
+    if out is None:
+        out = torch.empty((num_seqs, hq, d), dtype=out_dtype, device=q.device)
+    need = paged_attention_workspace_bytes(num_seqs, hq, d, max_context_len, partition_size)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib().paged_attention_append_decode(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        max_blocks, _ptr(context_lens), num_seqs, hq, int(max_context_len), float(scale), _ptr(out),
+        _DTYPE_CODE.get(out.dtype, -1), ctypes.byref(desc), int(partition_size), _ptr(workspace), ws_bytes,
+        _stream(stream)), "paged_attention_append_decode")
+    return out
+
+
 def paged_attention_decode_static(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                                   block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                                   out: torch.Tensor, max_context_len: int, partition_size: int = 0,
@@ -217,6 +256,38 @@ def copy_blocks(k_caches: torch.Tensor | Sequence[torch.Tensor], v_caches: torch
     varr = (ctypes.c_void_p * n)(*[t.data_ptr() for t in v_caches])
     _check(_lib().copy_blocks(karr, varr, n, _ptr(src_dst_pairs), src_dst_pairs.numel() // 2, ctypes.byref(desc),
                               _stream(stream)), "copy_blocks")
+
+
+def _ptr_array(ts):
+    return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+
+
+def swap_blocks(src_k: torch.Tensor | Sequence[torch.Tensor], src_v: torch.Tensor | Sequence[torch.Tensor],
+                dst_k: torch.Tensor | Sequence[torch.Tensor], dst_v: torch.Tensor | Sequence[torch.Tensor],
+                src_dst_pairs: torch.Tensor, stream=None) -> None:
+    """Move whole blocks src -> dst between two pools (GPU or pinned host memory), every layer, K and V."""
+    src_k, src_v, dst_k, dst_v = ([t] if isinstance(t, torch.Tensor) else list(t) for t in (src_k, src_v, dst_k, dst_v))
+    _require(len(src_k) == len(src_v) == len(dst_k) == len(dst_v) > 0, "one K and one V pool per layer on each side")
+    for t in (*src_k, *src_v, *dst_k, *dst_v):
+        _require(t.is_contiguous() and (t.is_cuda or t.is_pinned()), "pools must be contiguous, on the GPU or pinned")
+    _require(src_dst_pairs.dtype == torch.int64 and src_dst_pairs.numel() % 2 == 0, "src_dst_pairs: int64 [n, 2]")
+    _require(src_dst_pairs.is_cuda or src_dst_pairs.is_pinned(), "src_dst_pairs must be GPU-addressable")
+    desc = cache_desc(src_k[0])
+    _check(_lib().swap_blocks(_ptr_array(src_k), _ptr_array(src_v), src_k[0].shape[0], _ptr_array(dst_k),
+                              _ptr_array(dst_v), dst_k[0].shape[0], len(src_k), _ptr(src_dst_pairs),
+                              src_dst_pairs.numel() // 2, ctypes.byref(desc), _stream(stream)), "swap_blocks")
+
+
+def compact_tokens(src_slots: torch.Tensor, dst_slots: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   stream=None) -> None:
+    """Move the K/V rows of every head from slot src_slots[i] to slot dst_slots[i]."""
+    for t in (src_slots, dst_slots, k_cache, v_cache):
+        _require(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    _require(src_slots.dtype == torch.int64 and dst_slots.dtype == torch.int64 and
+             src_slots.numel() == dst_slots.numel(), "src_slots/dst_slots: int64 of equal length")
+    desc = cache_desc(k_cache)
+    _check(_lib().compact_tokens(_ptr(src_slots), _ptr(dst_slots), src_slots.numel(), _ptr(k_cache), _ptr(v_cache),
+                                 ctypes.byref(desc), _stream(stream)), "compact_tokens")
 
 
 def check_device_error(stream=None) -> int:

@@ -15,8 +15,20 @@ Administration", "How PagedAttention Works", steps 3-4):
 * ``free`` drops a sequence's references; blocks at count 0 return to the
   free list.
 
+* ``swap_out`` / ``swap_in`` move a whole sequence between a GPU pool's
+  manager and a host pool's manager (tonho.wtf "vllm", "como funciona":
+  eviction is all-or-nothing per sequence, and a sequence comes back by swap
+  from CPU RAM) and return the (src, dst) block pairs for ``swap_blocks``;
+* ``needs_compaction`` / ``compact`` implement the trigger and the target
+  allocation of token-level compaction (gist.science "Zipage", Compressed
+  PagedAttention: a request may hold at most N_max blocks; when it has N_max
+  and the last is full, the tokens it keeps are written into fresh target
+  blocks, at most N_max - 1 of them, so that blocks shared with other
+  requests stay intact) and return the (src slot, dst slot) pairs for
+  ``compact_tokens``.  Which tokens to keep is the caller's choice.
+
 The kernels never see this object: it produces the slot mapping, the block
-tables and the copy-on-write pairs that the C ABI consumes.
+tables and the copy pairs that the C ABI consumes.
 """
 from __future__ import annotations
 
@@ -49,6 +61,7 @@ class BlockManager:
             self._free = order[::-1]  # pop() takes free_order[0] first
         self.refcount = [0] * num_blocks
         self._seqs: dict[int, _Seq] = {}
+        self._deferred: list[int] = []
 
     # -- queries ---------------------------------------------------------
     @property
@@ -130,3 +143,76 @@ class BlockManager:
             self.refcount[b] -= 1
             if self.refcount[b] == 0:
                 self._free.append(b)
+
+    # -- token-level compaction ----------------------------------------------
+    def needs_compaction(self, seq: int, n_max: int) -> bool:
+        """True when the sequence holds n_max blocks (or more) and its last block is full."""
+        s = self._seqs[seq]
+        return len(s.table) >= n_max and s.num_tokens % self.block_size == 0 and s.num_tokens > 0
+
+    def compact(self, seq: int, keep_positions, defer_free: bool = False) -> tuple[list[int], list[int]]:
+        """Rewrite the kept token positions (ascending) into fresh target blocks.
+
+        The sequence's table becomes the target blocks and its length the
+        number of kept tokens; its old blocks lose one reference each (blocks
+        still shared with other sequences stay).  Returns (src_slots,
+        dst_slots) for compact_tokens.  With defer_free, blocks that drop to
+        zero references stay out of the free list until release_deferred():
+        several compactions can then share one compact_tokens launch without
+        a later one's targets landing on an earlier one's sources.
+        """
+        s = self._seqs[seq]
+        keep = [int(p) for p in keep_positions]
+        if any(b <= a for a, b in zip(keep, keep[1:])) or (keep and not 0 <= keep[0] <= keep[-1] < s.num_tokens):
+            raise ValueError("keep_positions must be ascending positions of the sequence")
+        bs = self.block_size
+        targets = [self._take() for _ in range((len(keep) + bs - 1) // bs)]
+        src = [s.table[p // bs] * bs + p % bs for p in keep]
+        dst = [targets[i // bs] * bs + i % bs for i in range(len(keep))]
+        for b in s.table:
+            self.refcount[b] -= 1
+            if self.refcount[b] == 0:
+                (self._deferred if defer_free else self._free).append(b)
+        s.table = targets
+        s.num_tokens = len(keep)
+        return src, dst
+
+    def release_deferred(self) -> int:
+        """Return the blocks held back by compact(defer_free=True) to the free list."""
+        n = len(self._deferred)
+        self._free.extend(self._deferred)
+        self._deferred.clear()
+        return n
+
+
+def swap_out(gpu: BlockManager, cpu: BlockManager, seq: int) -> list[tuple[int, int]]:
+    """Move a sequence from the GPU pool's manager to the host pool's manager.
+
+    Every block of the sequence gets a host block; the GPU blocks lose the
+    sequence's reference.  Returns the (gpu block, host block) pairs to copy
+    with swap_blocks before the GPU blocks are reused.
+    """
+    return _move(gpu, cpu, seq)
+
+
+def swap_in(cpu: BlockManager, gpu: BlockManager, seq: int) -> list[tuple[int, int]]:
+    """Bring a swapped-out sequence back; returns the (host block, gpu block) pairs."""
+    return _move(cpu, gpu, seq)
+
+
+def _move(src: BlockManager, dst: BlockManager, seq: int) -> list[tuple[int, int]]:
+    if src.block_size != dst.block_size:
+        raise ValueError("pools must use the same block size")
+    n = src.num_tokens(seq)
+    table = src.block_table(seq)
+    if dst.num_free < len(table):
+        raise OutOfBlocks("destination pool full")
+    dst.add_sequence(seq)
+    dst._seqs[seq].num_tokens = n
+    pairs = []
+    for b in table:
+        nb = dst._take()
+        dst._seqs[seq].table.append(nb)
+        pairs.append((b, nb))
+    src.free(seq)
+    return pairs

@@ -66,6 +66,35 @@ static pkv_status encode_cache_map(CUtensorMap* m, const void* base, const pkv_c
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_INVALID_ARG;
 }
 
+// Workspace of a split-K call: the fused merge's arrival counters (one per
+// sequence and query head, an upper bound on the head groups), then the
+// partial outputs [B][Hq][parts][D] and log-sum-exps [B][Hq][parts], each
+// region 256-byte aligned.
+struct WorkspaceLayout {
+    int64_t ctr_off, o_off, lse_off, total;
+};
+
+static int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
+
+static WorkspaceLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim, int64_t parts) {
+    WorkspaceLayout w;
+    const int64_t rows = num_seqs * num_q_heads * parts;
+    w.ctr_off = 0;
+    w.o_off = round256(num_seqs * num_q_heads * 8);
+    w.lse_off = w.o_off + round256(rows * head_dim * 4);
+    w.total = w.lse_off + round256(rows * 4);
+    return w;
+}
+
+// Epoch of a decode call: a process-wide counter, 48 bits, never 0.
+static std::atomic<unsigned long long> g_epoch{0};
+static unsigned long long next_epoch() {
+    for (;;) {
+        const unsigned long long e = (g_epoch.fetch_add(1) + 1) & ((1ull << 48) - 1);
+        if (e != 0) return e;
+    }
+}
+
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Shape checks common to every call on a cache.
@@ -169,10 +198,8 @@ size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, in
     const int64_t P = partition_size == 0 ? kAutoPartition : partition_size;  // auto never goes below 512
     const int64_t parts = max_context_len == 0 ? 1 : (max_context_len + P - 1) / P;
     if (parts <= 1) return 0;
-    const int64_t rows = (int64_t)num_seqs * num_q_heads * parts;
-    const int64_t o_bytes = ((rows * head_dim * 4) + 255) / 256 * 256;
-    const int64_t lse_bytes = ((rows * 4) + 255) / 256 * 256;
-    return (size_t)(o_bytes + lse_bytes);
+    const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, head_dim, parts);
+    return (size_t)w.total;
 }
 
 int32_t paged_attention_partition_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
@@ -185,12 +212,16 @@ int32_t paged_attention_partition_size(int32_t num_seqs, int32_t num_q_heads, in
     return resolve_partition(partition_size, (int64_t)num_seqs * num_kv_heads * head_tiles, max_context_len);
 }
 
-pkv_status paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
-                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                  const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
-                                  int32_t max_context_len, float scale, void* out, int32_t out_dtype,
-                                  const pkv_cache_desc* cache, int32_t partition_size, void* workspace,
-                                  size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+// paged_attention_decode, optionally with the block write of one new token
+// per sequence fused in (k_new != nullptr).
+static pkv_status decode_impl(const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                              const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                              int32_t num_q_heads, int32_t max_context_len, float scale, void* out,
+                              int32_t out_dtype, const pkv_cache_desc* cache, int32_t partition_size,
+                              void* workspace, size_t workspace_bytes, void* stream) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
     if (cache->head_dim != kHeadDim) return PKV_ERR_UNSUPPORTED;
@@ -214,6 +245,10 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+    const bool fused_append = k_new != nullptr;
+    if (fused_append && (!v_new || !slot_mapping || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+                         !aligned(slot_mapping, 8)))
         return PKV_ERR_INVALID_ARG;
 
     const int P = resolve_partition(partition_size, (int64_t)num_seqs * cache->num_kv_heads * head_tiles,
@@ -239,10 +274,13 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
     p.context_lens = context_lens;
     p.out = out;
     if (split) {
-        const int64_t rows = (int64_t)num_seqs * num_q_heads * max_parts;
-        const int64_t o_bytes = ((rows * kHeadDim * 4) + 255) / 256 * 256;
-        p.part_o = static_cast<float*>(workspace);
-        p.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+        const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, kHeadDim, max_parts);
+        char* base = static_cast<char*>(workspace);
+        p.merge_ctr = reinterpret_cast<unsigned long long*>(base + w.ctr_off);
+        p.part_o = reinterpret_cast<float*>(base + w.o_off);
+        p.part_lse = reinterpret_cast<float*>(base + w.lse_off);
+        p.fuse_merge = max_parts <= kFuseMergeMaxParts ? 1 : 0;
+        p.epoch = next_epoch();
     }
     p.err = err;
     p.num_blocks = cache->num_blocks;
@@ -258,6 +296,14 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
     p.out_dtype = out_dtype;
     p.split = split ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
+    if (fused_append) {
+        p.fused_append = 1;
+        p.k_new = static_cast<const uint4*>(k_new);
+        p.v_new = static_cast<const uint4*>(v_new);
+        p.slot_mapping = slot_mapping;
+        p.k_cache = static_cast<uint4*>(const_cast<void*>(k_cache));
+        p.v_cache = static_cast<uint4*>(const_cast<void*>(v_cache));
+    }
     int launches = 0;
     const cudaError_t e =
         launch_decode(p, cache->dtype, cache->block_size, tmk, tmv, static_cast<cudaStream_t>(stream), &launches);
@@ -265,16 +311,21 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-pkv_status copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
-                       const int64_t* src_dst_pairs, int32_t num_pairs, const pkv_cache_desc* cache,
-                       void* stream) {
+// Shared by copy_blocks and swap_blocks: whole blocks from a source pool to
+// a destination pool (which are the same pool for copy_blocks).
+static pkv_status move_blocks(void* const* src_k, void* const* src_v, int64_t src_blocks, void* const* dst_k,
+                              void* const* dst_v, int64_t dst_blocks, int32_t num_layers,
+                              const int64_t* src_dst_pairs, int32_t num_pairs, const pkv_cache_desc* cache,
+                              int err_code, void* stream) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
-    if (num_layers < 0 || num_pairs < 0) return PKV_ERR_INVALID_ARG;
+    if (num_layers < 0 || num_pairs < 0 || src_blocks < 1 || dst_blocks < 1) return PKV_ERR_INVALID_ARG;
     if (num_layers == 0 || num_pairs == 0) return PKV_OK;
-    if (!k_caches || !v_caches || !src_dst_pairs || !aligned(src_dst_pairs, 8)) return PKV_ERR_INVALID_ARG;
+    if (!src_k || !src_v || !dst_k || !dst_v || !src_dst_pairs || !aligned(src_dst_pairs, 8))
+        return PKV_ERR_INVALID_ARG;
     for (int l = 0; l < num_layers; ++l)
-        if (!k_caches[l] || !v_caches[l] || !aligned(k_caches[l], 16) || !aligned(v_caches[l], 16))
+        if (!src_k[l] || !src_v[l] || !dst_k[l] || !dst_v[l] || !aligned(src_k[l], 16) || !aligned(src_v[l], 16) ||
+            !aligned(dst_k[l], 16) || !aligned(dst_v[l], 16))
             return PKV_ERR_INVALID_ARG;
     const int64_t block_bytes = (int64_t)cache->num_kv_heads * cache->block_size * cache->head_dim * 2;
     if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
@@ -288,17 +339,95 @@ pkv_status copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num
         CopyParams p;
         std::memset(&p, 0, sizeof(p));
         p.err = err;
+        p.err_code = err_code;
         p.num_layers = num_layers - l0 < kCopyMaxLayers ? num_layers - l0 : kCopyMaxLayers;
         for (int l = 0; l < p.num_layers; ++l) {
-            p.k[l] = static_cast<uint4*>(k_caches[l0 + l]);
-            p.v[l] = static_cast<uint4*>(v_caches[l0 + l]);
+            p.src_k[l] = static_cast<const uint4*>(src_k[l0 + l]);
+            p.src_v[l] = static_cast<const uint4*>(src_v[l0 + l]);
+            p.dst_k[l] = static_cast<uint4*>(dst_k[l0 + l]);
+            p.dst_v[l] = static_cast<uint4*>(dst_v[l0 + l]);
         }
         p.pairs = src_dst_pairs;
-        p.num_blocks = cache->num_blocks;
+        p.src_blocks = src_blocks;
+        p.dst_blocks = dst_blocks;
         p.block_vecs = block_vecs;
         p.num_pairs = num_pairs;
         e = launch_copy_blocks(p, static_cast<cudaStream_t>(stream), &launches);
     }
+    g_launches += launches;
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" {
+
+pkv_status paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_context_len, float scale, void* out, int32_t out_dtype,
+                                  const pkv_cache_desc* cache, int32_t partition_size, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    return decode_impl(q, nullptr, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, num_q_heads, max_context_len, scale, out, out_dtype, cache,
+                       partition_size, workspace, workspace_bytes, stream);
+}
+
+pkv_status paged_attention_append_decode(const void* q, const void* k_new, const void* v_new,
+                                         const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_context_len, float scale, void* out, int32_t out_dtype,
+                                         const pkv_cache_desc* cache, int32_t partition_size, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+    if (num_seqs > 0 && !k_new) return PKV_ERR_INVALID_ARG;
+    return decode_impl(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, num_q_heads, max_context_len, scale, out, out_dtype, cache,
+                       partition_size, workspace, workspace_bytes, stream);
+}
+
+pkv_status copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                       const int64_t* src_dst_pairs, int32_t num_pairs, const pkv_cache_desc* cache,
+                       void* stream) {
+    if (!cache) return PKV_ERR_INVALID_ARG;
+    return move_blocks(k_caches, v_caches, cache->num_blocks, k_caches, v_caches, cache->num_blocks, num_layers,
+                       src_dst_pairs, num_pairs, cache, PKV_DEVERR_COPY_ID, stream);
+}
+
+pkv_status swap_blocks(void* const* src_k_caches, void* const* src_v_caches, int64_t src_num_blocks,
+                       void* const* dst_k_caches, void* const* dst_v_caches, int64_t dst_num_blocks,
+                       int32_t num_layers, const int64_t* src_dst_pairs, int32_t num_pairs,
+                       const pkv_cache_desc* cache, void* stream) {
+    return move_blocks(src_k_caches, src_v_caches, src_num_blocks, dst_k_caches, dst_v_caches, dst_num_blocks,
+                       num_layers, src_dst_pairs, num_pairs, cache, PKV_DEVERR_COPY_ID, stream);
+}
+
+pkv_status compact_tokens(const int64_t* src_slots, const int64_t* dst_slots, int64_t num_tokens, void* k_cache,
+                          void* v_cache, const pkv_cache_desc* cache, void* stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!src_slots || !dst_slots || !k_cache || !v_cache || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(src_slots, 8) || !aligned(dst_slots, 8))
+        return PKV_ERR_INVALID_ARG;
+    const int row_vecs = cache->head_dim * 2 / 16;
+    const int64_t total = num_tokens * cache->num_kv_heads * row_vecs;
+    if (total / num_tokens != (int64_t)cache->num_kv_heads * row_vecs || (total + 255) / 256 > INT_MAX)
+        return PKV_ERR_INVALID_ARG;
+    int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+    CompactParams p;
+    p.err = err;
+    p.src_slots = src_slots;
+    p.dst_slots = dst_slots;
+    p.k_cache = static_cast<uint4*>(k_cache);
+    p.v_cache = static_cast<uint4*>(v_cache);
+    p.num_tokens = num_tokens;
+    p.num_slots = cache->num_blocks * cache->block_size;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.block_size = cache->block_size;
+    p.row_vecs = row_vecs;
+    int launches = 0;
+    const cudaError_t e = launch_compact(p, static_cast<cudaStream_t>(stream), &launches);
     g_launches += launches;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -52,7 +52,7 @@ struct DecodeSmem {
     static constexpr int kRingBytes = ((kStagesBytes > kRedBytes ? kStagesBytes : kRedBytes) + 1023) / 1024 * 1024;
     static constexpr int kBarOffset = kRingBytes;
     static constexpr int kFlagOffset = kBarOffset + 2 * NST * 8;
-    static constexpr int kTotal = kFlagOffset + 16;
+    static constexpr int kTotal = kFlagOffset + 16;  // flags[0]: errors, flags[1]: last-arrival verdict
     static constexpr int kDynamic = kTotal + 1024;        // slack to align the base to 1024 B
 };
 
@@ -64,6 +64,81 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int s, int h, i
         static_cast<__nv_bfloat16*>(p.out)[i] = __float2bfloat16_rn(v);
     else
         static_cast<__half*>(p.out)[i] = __float2half_rn(v);
+}
+
+// Count one arrival of this call (epoch) on a (epoch << 16 | count) counter
+// and report whether it was the nparts-th.  A counter left by another call
+// (different epoch) counts as zero, so stale or garbage contents never
+// matter; the last arrival also resets the count, so a replay of the same
+// launch (same epoch, e.g. from a captured graph) starts from zero too.
+// Lock-free: a failed CAS means another CTA's arrival got in first, so the
+// loop ends after at most nparts tries.
+__device__ __forceinline__ bool arrive_last(unsigned long long* ctr, unsigned long long epoch, int nparts) {
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
+    for (;;) {
+        const unsigned long long cnt = (old >> 16) == epoch ? (old & 0xFFFFull) + 1 : 1;
+        const bool last = cnt == (unsigned long long)nparts;
+        const unsigned long long prev = atomicCAS(ctr, old, (epoch << 16) | (last ? 0ull : cnt));
+        if (prev == old) return last;
+        old = prev;
+    }
+}
+
+// Merge the nparts partial (o_p, lse_p) of query heads h0 .. h0+rows-1 of
+// sequence s into out: out = sum_p 2^(lse_p - LSE) o_p, LSE = log2 sum_p
+// 2^lse_p.  A partition marked +inf (bad metadata) zeroes the row.  Runs in
+// the CTA that arrived last, so it sits on the critical path of the row: all
+// loads of a phase are issued together (L2 latency once per phase, not once
+// per partition).  Partials written by other CTAs are read through L2
+// (ld.global.cg).  `w` is shared scratch of rows x (kFuseMergeMaxParts + 1)
+// floats.
+__device__ __noinline__ void merge_row_partials(const DecodeParams& p, int s, int h0, int rows, int nparts,
+                                                float* w) {
+    constexpr int MP = kFuseMergeMaxParts;
+    const int tid = threadIdx.x;
+    const int64_t row0 = (int64_t)s * p.num_q_heads + h0;
+    for (int i = tid; i < rows * nparts; i += blockDim.x) {
+        const int r = i / nparts, j = i - r * nparts;
+        w[r * MP + j] = __ldcg(p.part_lse + (row0 + r) * p.max_parts + j);
+    }
+    __syncthreads();
+    for (int r = tid; r < rows; r += blockDim.x) {
+        float M = -INFINITY;
+        for (int j = 0; j < nparts; ++j) M = fmaxf(M, w[r * MP + j]);
+        const bool bad = M == INFINITY;  // a bad row merges to exact zeros
+        float sum = 0.f;
+        for (int j = 0; j < nparts; ++j) {
+            const float e = bad ? 0.f : exp2f(w[r * MP + j] - M);
+            w[r * MP + j] = e;
+            sum += e;
+        }
+        w[rows * MP + r] = bad ? 0.f : 1.f / sum;
+    }
+    __syncthreads();
+    // one float4 of one row per item; every partition's load issued up front
+    for (int i = tid; i < rows * (kHeadDim / 4); i += blockDim.x) {
+        const int r = i / (kHeadDim / 4), c = i - r * (kHeadDim / 4);
+        const float4* po = reinterpret_cast<const float4*>(p.part_o + (row0 + r) * p.max_parts * kHeadDim) + c;
+        float4 v[MP];
+#pragma unroll
+        for (int j = 0; j < MP; ++j)
+            if (j < nparts) v[j] = __ldcg(po + j * (kHeadDim / 4));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < MP; ++j)
+            if (j < nparts) {
+                const float wj = w[r * MP + j];
+                acc.x += wj * v[j].x;
+                acc.y += wj * v[j].y;
+                acc.z += wj * v[j].z;
+                acc.w += wj * v[j].w;
+            }
+        const float inv = w[rows * MP + r];
+        store_out(p, s, h0 + r, 4 * c, acc.x * inv);
+        store_out(p, s, h0 + r, 4 * c + 1, acc.y * inv);
+        store_out(p, s, h0 + r, 4 * c + 2, acc.z * inv);
+        store_out(p, s, h0 + r, 4 * c + 3, acc.w * inv);
+    }
 }
 
 // Tunables (compile-time): consumer warps per CTA, ring stages for 16- and
@@ -84,7 +159,7 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int s, int h, i
 
 // NH: 8-head n-tiles per CTA (1: up to 8 query heads of a group, 2: up to 16).
 template <bool kBF16, int BS, int NH, int NCW, int NST>
-__global__ void __launch_bounds__((NCW + 1) * 32, PKV_MINB)
+__global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB - 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeParams p) {
     using S = DecodeSmem<BS, NCW, NST, 8 * NH>;
@@ -106,7 +181,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, PKV_MINB)
     const int h0 = kvh * p.group + ht * HT;  // first query head of this CTA
     const int rows = min(HT, p.group - ht * HT);
 
-    const int L = __ldg(p.context_lens + s);
+    // Launched with programmatic stream serialisation: the previous kernel on
+    // the stream (e.g. the block write) may still be running.  Let the next
+    // kernel start launching, then wait for the previous one to finish before
+    // reading anything it may have written.
+    pdl_launch_dependents();
+    if (tid == 32 * NCW) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+    }
+    pdl_wait();
+
+    const int L = p.context_lens[s];
     const bool bad_len = L < 0 || L > p.len_limit;
     if (bad_len || part * p.partition_size >= L) {
         // Partition 0 owns the output of a sequence with nothing to attend
@@ -155,12 +241,32 @@ __global__ void __launch_bounds__((NCW + 1) * 32, PKV_MINB)
 
     if (warp == NCW) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            prefetch_tensormap(&tmk);
-            prefetch_tensormap(&tmv);
-        }
         const uint64_t policy = l2_policy_evict_first();
         const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks_per_seq + blk0;
+        if (p.fused_append && tok1 == L) {
+            // Block write fused into the decode: this partition holds the last
+            // position, so this CTA writes that token's row for its KV head
+            // before any TMA load can read it.
+            const int64_t slot = p.slot_mapping[s];
+            if (slot >= 0) {
+                const int pos = L - 1;
+                const int pb = p.block_tables[(int64_t)s * p.max_blocks_per_seq + pos / BS];
+                if (pb >= 0 && (int64_t)pb < p.num_blocks) {  // a bad id is reported by the loads below
+                    if (slot == (int64_t)pb * BS + pos % BS) {
+                        const int64_t row = ((int64_t)pb * p.num_kv_heads + kvh) * BS + pos % BS;
+                        const int64_t src = ((int64_t)s * p.num_kv_heads + kvh) * (kHeadDim / 8);
+                        if (lane < 16)
+                            p.k_cache[row * (kHeadDim / 8) + lane] = p.k_new[src + lane];
+                        else
+                            p.v_cache[row * (kHeadDim / 8) + lane - 16] = p.v_new[src + lane - 16];
+                        fence_proxy_async_global();
+                    } else if (lane == 0) {
+                        record_error(p.err, PKV_DEVERR_SLOT);
+                    }
+                }
+                __syncwarp();
+            }
+        }
         bool ok = true;
         for (int c = 0; c < nblk; c += 32) {
             const int j = c + lane;
@@ -423,37 +529,77 @@ __global__ void __launch_bounds__((NCW + 1) * 32, PKV_MINB)
             store_out(p, s, h, d, bad ? 0.f : o / lsum);
         }
     }
+
+    if (write_partial && p.fuse_merge) {
+        // Every partition of this (sequence, head group) arrives on its
+        // counter once its partials are globally visible; the last to arrive
+        // merges them.  Nothing ever waits for another CTA.
+        __threadfence();
+        __syncthreads();
+        if (tid == 0)
+            flags[1] = arrive_last(p.merge_ctr + (int64_t)s * gridDim.y + blockIdx.y, p.epoch, nparts) ? 1 : 0;
+        __syncthreads();
+        if (flags[1]) {
+            __threadfence();
+            merge_row_partials(p, s, h0, rows, nparts, reinterpret_cast<float*>(smem));
+        }
+    }
 }
 
-// Split-K merge: out = sum_p 2^(lse_p - LSE) o_p with LSE = log2 sum_p 2^lse_p,
-// for sequences with at least two partitions.  One CTA per (query head,
-// sequence); thread d owns output column d.
-__global__ void __launch_bounds__(kHeadDim) reduce_kernel(const DecodeParams p) {
-    const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
-    const int L = __ldg(p.context_lens + s);
+// Split-K merge for sequences with many partitions (the decode kernel merges
+// the others itself): out = sum_p 2^(lse_p - LSE) o_p, LSE = log2 sum_p
+// 2^lse_p.  One CTA per (query head, sequence); kReduceGroups groups of 128
+// threads take interleaved partitions, thread d of a group owns column d,
+// and the groups combine through shared memory.
+constexpr int kReduceGroups = 4;
+
+__global__ void __launch_bounds__(kHeadDim * kReduceGroups) reduce_kernel(const DecodeParams p) {
+    pdl_wait();  // the decode kernel's partials must be complete
+    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
+    const int d = tid % kHeadDim, grp = tid / kHeadDim;
+    const int L = p.context_lens[s];
     if (L < 0 || L > p.len_limit) return;  // the decode kernel already zeroed it
     const int np = (L + p.partition_size - 1) / p.partition_size;
     if (np <= 1) return;                   // written directly by the decode kernel
     const int64_t base = ((int64_t)s * p.num_q_heads + h) * p.max_parts;
     const float* lse = p.part_lse + base;
     const float* po = p.part_o + base * kHeadDim + d;
+    __shared__ float red_m[kHeadDim * kReduceGroups / 32];
+    __shared__ float red_acc[kReduceGroups][kHeadDim];
+    __shared__ float red_sum[kReduceGroups];
+    // block-wide max of lse (+inf, the bad-metadata mark, wins and zeroes the row)
     float M = -INFINITY;
-    bool bad = false;
-    for (int i = 0; i < np; ++i) {
-        const float v = lse[i];
-        bad |= v == INFINITY;
-        M = fmaxf(M, v);
+    for (int i = tid; i < np; i += blockDim.x) M = fmaxf(M, lse[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if ((tid & 31) == 0) red_m[tid >> 5] = M;
+    __syncthreads();
+    M = red_m[0];
+#pragma unroll
+    for (int i = 1; i < kHeadDim * kReduceGroups / 32; ++i) M = fmaxf(M, red_m[i]);
+    if (M == INFINITY) {
+        if (grp == 0) store_out(p, s, h, d, 0.f);
+        return;
     }
     float acc = 0.f, sum = 0.f;
-    if (!bad) {
-#pragma unroll 8
-        for (int i = 0; i < np; ++i) {
-            const float w = exp2f(lse[i] - M);
-            sum += w;
-            acc += w * po[(int64_t)i * kHeadDim];
-        }
+#pragma unroll 4
+    for (int i = grp; i < np; i += kReduceGroups) {
+        const float w = exp2f(lse[i] - M);
+        sum += w;
+        acc += w * po[(int64_t)i * kHeadDim];
     }
-    store_out(p, s, h, d, bad ? 0.f : acc / sum);
+    red_acc[grp][d] = acc;
+    if (d == 0) red_sum[grp] = sum;
+    __syncthreads();
+    if (grp == 0) {
+        float a = 0.f, t = 0.f;
+#pragma unroll
+        for (int g = 0; g < kReduceGroups; ++g) {
+            a += red_acc[g][d];
+            t += red_sum[g];
+        }
+        store_out(p, s, h, d, a / t);
+    }
 }
 
 template <bool kBF16, int BS, int NH>
@@ -466,13 +612,11 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmk
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kDynamic);
     if (e != cudaSuccess) return e;
     const dim3 grid(p.max_parts, p.num_kv_heads * p.head_tiles, p.num_seqs);
-    kern<<<grid, (NCW + 1) * 32, S::kDynamic, stream>>>(tmk, tmv, p);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, grid, dim3((NCW + 1) * 32), S::kDynamic, stream, tmk, tmv, p);
     if (e != cudaSuccess) return e;
     ++*launches;
-    if (p.split) {
-        reduce_kernel<<<dim3(p.num_q_heads, p.num_seqs), kHeadDim, 0, stream>>>(p);
-        e = cudaGetLastError();
+    if (p.split && !p.fuse_merge) {
+        e = launch_pdl(reduce_kernel, dim3(p.num_q_heads, p.num_seqs), dim3(kHeadDim * kReduceGroups), 0, stream, p);
         if (e != cudaSuccess) return e;
         ++*launches;
     }

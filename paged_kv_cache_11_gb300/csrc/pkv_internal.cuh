@@ -18,6 +18,13 @@ constexpr int kHeadDim = 128;          // supported head_dim
 constexpr int kAutoPartition = 512;    // smallest automatic split-K partition (tokens)
 constexpr int kDecodeCtasPerSm = 5;    // resident decode CTAs per SM the kernel is tuned for
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on any in-CTA wait (2 s)
+// Split-K calls with at most this many partitions per sequence merge inside
+// the decode kernel (the last partition to finish merges); longer ones use
+// the separate merge kernel.
+#ifndef PKV_FUSE_MERGE_MAX_PARTS
+#define PKV_FUSE_MERGE_MAX_PARTS 16
+#endif
+constexpr int kFuseMergeMaxParts = PKV_FUSE_MERGE_MAX_PARTS;
 
 // The per-device error word lives in the API translation unit; kernels get
 // its device address as a parameter.  First error wins (atomicCAS from 0).
@@ -34,6 +41,21 @@ struct DecodeParams {
     float* part_o;               // [B][Hq][max_parts][D]   (split only)
     float* part_lse;             // [B][Hq][max_parts], log2 domain (split only)
     int* err;                    // device error word
+    // fused merge: one 64-bit arrival counter per (sequence, head group),
+    // holding (epoch << 16) | arrivals; a counter whose epoch is not this
+    // call's counts as zero, so the counters never need clearing.
+    unsigned long long* merge_ctr;  // [B][Hkv * head_tiles]
+    unsigned long long epoch;       // this call's epoch, 1 .. 2^48 - 1
+    int fuse_merge;                 // 1: the last partition of a row merges
+    // fused block write (paged_attention_append_decode): sequence s's new
+    // token, k_new/v_new [B][Hkv][D], goes to slot_mapping[s], which must be
+    // the slot of its last context position
+    const uint4* k_new;
+    const uint4* v_new;
+    const int64_t* slot_mapping;
+    uint4* k_cache;
+    uint4* v_cache;
+    int fused_append;
     int64_t num_blocks;
     int num_seqs, num_q_heads, num_kv_heads;
     int max_blocks_per_seq;
@@ -67,21 +89,71 @@ struct AppendParams {
 };
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream, int* launches);
 
-constexpr int kCopyMaxLayers = 64;
+// Whole-block moves between two pools (the same pool for copy-on-write
+// copies; a GPU pool and a host pool for swapping), up to kCopyMaxLayers
+// layers per launch.
+constexpr int kCopyMaxLayers = 32;
 struct CopyParams {
     int* err;
-    uint4* k[kCopyMaxLayers];
-    uint4* v[kCopyMaxLayers];
-    const int64_t* pairs;
-    int64_t num_blocks;
-    int64_t block_vecs;  // 16-byte vectors per block of one cache
+    int err_code;                 // PKV_DEVERR_* recorded for an id outside a pool
+    const uint4* src_k[kCopyMaxLayers];
+    const uint4* src_v[kCopyMaxLayers];
+    uint4* dst_k[kCopyMaxLayers];
+    uint4* dst_v[kCopyMaxLayers];
+    const int64_t* pairs;         // [num_pairs][2] = (src, dst)
+    int64_t src_blocks, dst_blocks;
+    int64_t block_vecs;           // 16-byte vectors per block of one cache
     int num_layers, num_pairs;
 };
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream, int* launches);
 
+// Token-row moves inside one pool: rows of every KV head from slot src[i]
+// to slot dst[i] (compaction into fresh target blocks).
+struct CompactParams {
+    int* err;
+    const int64_t* src_slots;
+    const int64_t* dst_slots;
+    uint4* k_cache;
+    uint4* v_cache;
+    int64_t num_tokens;
+    int64_t num_slots;
+    int num_kv_heads, block_size, row_vecs;
+};
+cudaError_t launch_compact(const CompactParams& p, cudaStream_t stream, int* launches);
+
+// Launch a kernel with programmatic stream serialisation: it may start while
+// the previous kernel on the stream is still running, and must call
+// pdl_wait() before touching any memory that kernel could write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // Inline PTX
 // ---------------------------------------------------------------------------
+// Wait until the grid this one depends on has completed and its memory is
+// visible (returns at once when there is none).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Order this thread's generic-proxy global writes before later async-proxy
+// (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Allow the next kernel on the stream to start launching its CTAs.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -23,7 +23,12 @@ def to_bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def gpu_step(wl, device, partition_size: int = 0, out_dtype=torch.float32, max_context_len=None):
+def single_token_step(wl) -> bool:
+    """True when the step appends exactly one token per sequence, at its last position."""
+    return len(wl.cow_pairs) == 0 and np.array_equal(wl.append_seq, np.arange(wl.num_seqs))
+
+
+def gpu_step(wl, device, partition_size: int = 0, out_dtype=torch.float32, max_context_len=None, fused=False):
     import paged_kv_cache_11_gb300 as pkv
     dt = wl.dtype
     kc = to_dev(wl.k_cache, dt, device)
@@ -31,12 +36,20 @@ def gpu_step(wl, device, partition_size: int = 0, out_dtype=torch.float32, max_c
     q = to_dev(wl.q, dt, device)
     bt = torch.from_numpy(wl.block_tables).to(device)
     cl = torch.from_numpy(wl.context_lens).to(device)
+    mcl = wl.max_context_len if max_context_len is None else max_context_len
+    if fused:
+        assert single_token_step(wl)
+        out = pkv.paged_attention_append_decode(q, to_dev(wl.new_k, dt, device), to_dev(wl.new_v, dt, device),
+                                                torch.from_numpy(wl.slot_mapping).to(device), kc, vc, bt, cl,
+                                                wl.scale, max_context_len=mcl, partition_size=partition_size,
+                                                out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        return kc, vc, out
     if len(wl.cow_pairs):
         pkv.copy_blocks(kc, vc, torch.from_numpy(wl.cow_pairs).to(device))
     if len(wl.slot_mapping):
         pkv.paged_kv_append(to_dev(wl.new_k, dt, device), to_dev(wl.new_v, dt, device),
                             torch.from_numpy(wl.slot_mapping).to(device), kc, vc)
-    mcl = wl.max_context_len if max_context_len is None else max_context_len
     out = pkv.paged_attention_decode(q, kc, vc, bt, cl, wl.scale, max_context_len=mcl,
                                      partition_size=partition_size, out_dtype=out_dtype)
     torch.cuda.synchronize()

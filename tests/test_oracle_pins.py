@@ -238,3 +238,45 @@ def test_copy_blocks_copies_only_the_listed_blocks():
 def test_nan_bits_are_what_the_helpers_use():
     assert np.isnan(oracle.to_f64(np.array([NAN["bf16"]], np.uint16), "bf16")[0])
     assert np.isnan(oracle.to_f64(np.array([NAN["fp16"]], np.uint16), "fp16")[0])
+
+
+# ---------------------------------------------------------------- swap / compaction
+def test_swap_blocks_moves_exactly_the_listed_blocks_between_pools():
+    rng = np.random.default_rng(18)
+    hkv, bs, d = 2, 16, 128
+    gk, gv = random_bits(rng, (9, hkv, bs, d), "bf16"), random_bits(rng, (9, hkv, bs, d), "bf16")
+    hk, hv = random_bits(rng, (5, hkv, bs, d), "bf16"), random_bits(rng, (5, hkv, bs, d), "bf16")
+    h0k, h0v = hk.copy(), hv.copy()
+    bad = oracle.swap_blocks(gk, gv, hk, hv, np.array([[7, 0], [2, 3], [9, 1], [1, 5]]))
+    assert bad == 2                                  # src 9 (GPU pool of 9) and dst 5 (host pool of 5)
+    assert np.array_equal(hk[0], gk[7]) and np.array_equal(hk[3], gk[2])
+    assert np.array_equal(hv[0], gv[7]) and np.array_equal(hv[3], gv[2])
+    assert np.array_equal(hk[[1, 2, 4]], h0k[[1, 2, 4]]) and np.array_equal(hv[[1, 2, 4]], h0v[[1, 2, 4]])
+
+
+def test_compaction_moves_rows_and_attention_sees_only_the_kept_tokens():
+    """Decode over the compacted table equals attention restricted to the kept positions
+    (gist.science "Zipage": kept tokens are rewritten into fresh target blocks)."""
+    rng = np.random.default_rng(19)
+    case = paged_case(rng, [70], 8, 2, 16, dtype="bf16", pool_slack=6)
+    L = 70
+    keep = np.sort(rng.choice(L, 29, replace=False))
+    keep[-1] = L - 1                                   # the newest token is always kept
+    keep = np.unique(keep)
+    free = sorted(set(range(case["num_blocks"])) - set(case["block_tables"][0].tolist()))
+    targets = free[:(len(keep) + 15) // 16]
+    src = [int(case["block_tables"][0, p // 16]) * 16 + int(p) % 16 for p in keep]
+    dst = [targets[i // 16] * 16 + i % 16 for i in range(len(keep))]
+    kc, vc = case["k_cache"].copy(), case["v_cache"].copy()
+    assert oracle.compact(kc, vc, src, dst) == 0
+    for a, b in zip(src, dst):
+        assert np.array_equal(kc[b // 16, :, b % 16], case["k_cache"][a // 16, :, a % 16])
+        assert np.array_equal(vc[b // 16, :, b % 16], case["v_cache"][a // 16, :, a % 16])
+    bt = np.full((1, len(targets)), -1, np.int32)
+    bt[0] = targets
+    out, _ = oracle.decode(case["q"], kc, vc, bt, np.array([len(keep)], np.int32), SCALE, "bf16")
+    kept = dict(case)
+    kept["K"] = [case["K"][0][:, keep, :]]
+    kept["V"] = [case["V"][0][:, keep, :]]
+    kept["context_lens"] = np.array([len(keep)], np.int32)
+    np.testing.assert_allclose(out, sdpa_reference(kept, SCALE), rtol=0, atol=1e-12)

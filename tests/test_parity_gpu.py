@@ -14,14 +14,16 @@ import torch
 
 import oracle
 from paged_kv_cache_11_gb300 import workload as W
-from tests.step_helpers import gpu_step, max_abs_err, oracle_step, to_bits, to_dev
+from tests.step_helpers import gpu_step, max_abs_err, oracle_step, single_token_step, to_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 TOL = 5e-3
 
 
 def _check(wl, device, **kw):
-    wl.poison()
+    if not getattr(wl, "_poisoned", False):
+        wl.poison()
+        wl._poisoned = True
     kc, vc, out = gpu_step(wl, device, **kw)
     okc, ovc, ref = oracle_step(wl)
     assert np.array_equal(to_bits(kc), okc), "K pool differs after copy_blocks + append"
@@ -137,6 +139,31 @@ def test_split_k_matches_single_pass(gpu):
         assert (split - single).abs().max().item() <= 1e-5
 
 
+@pytest.mark.parametrize("P", [0, 64])  # fused merge / separate merge kernel
+def test_workspace_reuse_and_garbage(gpu, P):
+    """One workspace reused across calls and pre-filled with garbage gives the same bits."""
+    import paged_kv_cache_11_gb300 as pkv
+    wl = W.make_workload("llama8b", num_seqs=7, lens=("uniform", 300, 2500), seed=3)
+    dev = gpu
+    kc, vc, q = to_dev(wl.k_cache, "bf16", dev), to_dev(wl.v_cache, "bf16", dev), to_dev(wl.q, "bf16", dev)
+    bt, cl = torch.from_numpy(wl.block_tables).to(dev), torch.from_numpy(wl.context_lens).to(dev)
+    mcl = wl.max_context_len
+    need = pkv.paged_attention_workspace_bytes(wl.num_seqs, wl.num_q_heads, 128, mcl, P)
+    assert need > 0
+    outs = []
+    for fill in (0x00, 0xFF, 0x5A, None, None):
+        ws = torch.empty(need, dtype=torch.uint8, device=dev) if fill is not None or not outs else ws
+        if fill is not None:
+            ws.fill_(fill)
+        outs.append(pkv.paged_attention_decode(q, kc, vc, bt, cl, wl.scale, max_context_len=mcl, partition_size=P,
+                                               workspace=ws).clone())
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    ref, _ = oracle.decode(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale, "bf16",
+                           threads=8)
+    assert max_abs_err(outs[0], ref) <= TOL
+
+
 def test_shared_blocks_equal_copied_blocks(gpu):
     """Sequences mapping the group's shared prefix == the same sequences with private copies."""
     wl = W.make_workload("shared_prefix", groups=1, per_group=3, prefix=64, suffix=(32, 60), pool_blocks=64)
@@ -154,6 +181,40 @@ def test_shared_blocks_equal_copied_blocks(gpu):
     wl.block_tables, wl.k_cache, wl.v_cache = bt, k, v
     _, _, copied = gpu_step(wl, gpu)
     assert torch.equal(shared, copied)
+
+
+# ------------------------------------------------------------------ fused block write + decode
+@pytest.mark.parametrize("name,kw", [
+    ("tiny", {}),
+    ("llama8b", dict(num_seqs=6, lens=("uniform", 512, 2100))),
+    ("opt13b", dict(num_seqs=9, lens=("uniform", 1, 700))),
+    ("llama70b_long", dict(num_seqs=2, lens=("fixed", (3000, 1537)))),
+    ("tiny", dict(num_seqs=5, lens=("fixed", (1, 16, 17, 32, 33)), num_q_heads=32, num_kv_heads=2, pool_blocks=0)),
+])
+@pytest.mark.parametrize("P", [0, 64])
+def test_fused_append_decode(gpu, name, kw, P):
+    wl = W.make_workload(name, **kw)
+    assert single_token_step(wl)
+    _check(wl, gpu, fused=True, partition_size=P)
+    # bit-identical to the separate block write + decode
+    kc1, vc1, o1 = gpu_step(wl, gpu, partition_size=P)
+    kc2, vc2, o2 = gpu_step(wl, gpu, partition_size=P, fused=True)
+    assert torch.equal(o1, o2)
+    # the pools hold NaN poison, so compare bit patterns
+    assert np.array_equal(to_bits(kc1), to_bits(kc2)) and np.array_equal(to_bits(vc1), to_bits(vc2))
+
+
+def test_fused_append_rejects_a_slot_that_is_not_the_last_position(gpu):
+    import paged_kv_cache_11_gb300 as pkv
+    pkv.check_device_error()
+    wl = W.make_workload("llama8b", num_seqs=3, lens=("fixed", (40, 300, 17)))
+    wl.slot_mapping = wl.slot_mapping.copy()
+    wl.slot_mapping[1] -= 1                      # the position before the last one
+    kc, vc, _ = gpu_step(wl, gpu, fused=True)
+    assert pkv.check_device_error() == 1
+    kbits = to_bits(kc)
+    wrong = int(wl.slot_mapping[1])
+    assert np.array_equal(kbits[wrong // 16, :, wrong % 16], wl.k_cache[wrong // 16, :, wrong % 16])  # untouched
 
 
 # ------------------------------------------------------------------ errors

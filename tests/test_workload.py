@@ -195,3 +195,48 @@ def test_poison_touches_only_unused_slots_and_step_targets():
     kt, k0t = wl.k_cache.transpose(0, 2, 1, 3), k0.transpose(0, 2, 1, 3)
     assert np.array_equal(kt[keep], k0t[keep])
     assert (kt[~keep] == W.NAN_BITS["bf16"]).all()
+
+
+# ---------------------------------------------------------------- swap / compaction bookkeeping
+def test_swap_out_and_in_round_trip():
+    from paged_kv_cache_11_gb300.block_manager import swap_in, swap_out
+    gpu, cpu = BlockManager(16, 16, W.permutation(2, 2, 16)), BlockManager(8, 16)
+    gpu.add_sequence(0)
+    gpu.append_tokens(0, 50)                         # 4 blocks
+    t = gpu.block_table(0)
+    out_pairs = swap_out(gpu, cpu, 0)
+    assert [a for a, _ in out_pairs] == t and gpu.num_free == 16 and cpu.num_free == 4
+    assert cpu.num_tokens(0) == 50 and [b for _, b in out_pairs] == cpu.block_table(0)
+    in_pairs = swap_in(cpu, gpu, 0)
+    assert [a for a, _ in in_pairs] == [b for _, b in out_pairs] and cpu.num_free == 8
+    assert gpu.num_tokens(0) == 50 and len(gpu.block_table(0)) == 4
+    slot, cow = gpu.append_token(0)                  # the sequence continues where it stopped
+    assert cow is None and slot == gpu.block_table(0)[3] * 16 + 50 % 16
+
+
+def test_compaction_trigger_and_targets_leave_shared_blocks_intact():
+    bm = BlockManager(32, 16)
+    bm.add_sequence(0)
+    bm.append_tokens(0, 64)                          # 4 full blocks
+    bm.fork(0, 1)                                    # shared prompt
+    shared = bm.block_table(0)
+    bm.append_tokens(1, 16)                          # sequence 1: 5 blocks, last one full
+    assert bm.needs_compaction(1, 5) and not bm.needs_compaction(1, 6) and not bm.needs_compaction(0, 5)
+    keep = list(range(0, 80, 3))                     # 27 tokens -> 2 target blocks (<= N_max - 1)
+    src, dst = bm.compact(1, keep)
+    t = bm.block_table(1)
+    assert len(t) == 2 and bm.num_tokens(1) == 27 and not set(t) & set(shared)
+    assert src[0] == shared[0] * 16 and dst == [t[i // 16] * 16 + i % 16 for i in range(27)]
+    assert bm.block_table(0) == shared and all(bm.refcount[b] == 1 for b in shared)
+
+
+def test_deferred_free_keeps_compaction_sources_out_of_later_targets():
+    bm = BlockManager(12, 16)
+    for s in range(2):
+        bm.add_sequence(s)
+        bm.append_tokens(s, 48)                     # 3 blocks each
+    old = set(bm.block_table(0)) | set(bm.block_table(1))
+    src0, dst0 = bm.compact(0, range(0, 48, 2), defer_free=True)
+    src1, dst1 = bm.compact(1, range(0, 48, 2), defer_free=True)
+    assert not (set(d // 16 for d in dst0 + dst1) & old)
+    assert bm.release_deferred() == 6 and bm.num_free == 12 - 4
