@@ -528,10 +528,113 @@ def run_ours(args):
     return 0
 
 
+# ---------------------------------------------------------------- swap / compaction rows
+def _timed(fn, steps, stream):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_data_movement(args):
+    """--workload swap: every block of the llama8b batch swapped out to a
+    page-locked host pool and back in (swap_blocks), against one contiguous
+    cudaMemcpyAsync of the same bytes each way.  --workload compact: each
+    llama8b sequence keeps every other token, rewritten into fresh target
+    blocks (compact_tokens), against the measured HBM copy peak."""
+    import torch
+
+    import paged_kv_cache_11_gb300 as pkv
+    from paged_kv_cache_11_gb300 import _build, workload as W
+
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build_all()
+    pkv.binding._lib()
+    wl = W.make_workload("llama8b")
+    up = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+    kc, vc = up(wl.k_cache), up(wl.v_cache)
+    stream = torch.cuda.current_stream()
+    bs = wl.block_size
+    used = np.concatenate([wl.block_tables[s, :(int(L) + bs - 1) // bs] for s, L in enumerate(wl.context_lens)])
+    block_bytes = 2 * wl.num_kv_heads * bs * wl.head_dim * 2
+    peaks = measured_peaks()
+    steps = max(1, min(args.steps, 50))
+    l0 = pkv.launch_count()
+    if args.workload == "swap":
+        n = len(used)
+        hk = torch.empty((n,) + tuple(kc.shape[1:]), dtype=kc.dtype).pin_memory()
+        hv = torch.empty_like(hk).pin_memory()
+        out_pairs = torch.from_numpy(np.stack([used, np.arange(n)], 1).astype(np.int64)).to(dev)
+        in_pairs = torch.from_numpy(np.stack([np.arange(n), used], 1).astype(np.int64)).to(dev)
+        for _ in range(3):
+            pkv.swap_blocks(kc, vc, hk, hv, out_pairs)
+            pkv.swap_blocks(hk, hv, kc, vc, in_pairs)
+        t_out = _timed(lambda: pkv.swap_blocks(kc, vc, hk, hv, out_pairs), steps, stream)
+        t_in = _timed(lambda: pkv.swap_blocks(hk, hv, kc, vc, in_pairs), steps, stream)
+        nbytes = n * block_bytes
+        flat_d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        flat_h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        m_out = _timed(lambda: flat_h.copy_(flat_d, non_blocking=True), steps, stream)
+        m_in = _timed(lambda: flat_d.copy_(flat_h, non_blocking=True), steps, stream)
+        assert pkv.check_device_error() == 0
+        out_gbs, in_gbs = nbytes / t_out / 1e6, nbytes / t_in / 1e6
+        line = {"metric": "swap_blocks GB/s (GPU pool <-> page-locked host pool)", "value": min(out_gbs, in_gbs),
+                "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": 3, "higher_is_better": True,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": "swap", "blocks": n, "bytes_each_way": nbytes, "block_bytes": block_bytes,
+                           "source": "every block of the llama8b batch"},
+                "swap_out_gbs": out_gbs, "swap_in_gbs": in_gbs,
+                "roofline": {"bound": "c2c", "unit": "GB/s",
+                             "peak_out": nbytes / m_out / 1e6, "peak_in": nbytes / m_in / 1e6,
+                             "frac_out": out_gbs / (nbytes / m_out / 1e6), "frac_in": in_gbs / (nbytes / m_in / 1e6),
+                             "peak_source": "one contiguous cudaMemcpyAsync of the same bytes, measured here"},
+                "gpu_launches": pkv.launch_count() - l0}
+    else:
+        srcs, dsts = [], []
+        base = wl.num_blocks  # targets in a second pool half, so no target is a source
+        for s, L in enumerate(wl.context_lens):
+            keep = np.arange(0, int(L), 2)
+            t0 = len(dsts)
+            srcs += [int(wl.block_tables[s, p // bs]) * bs + int(p) % bs for p in keep]
+            dsts += [(base + (t0 + i) // bs) * bs + (t0 + i) % bs for i in range(len(keep))]
+        kc2 = torch.cat([kc, torch.empty_like(kc)])
+        vc2 = torch.cat([vc, torch.empty_like(vc)])
+        a = torch.tensor(srcs, dtype=torch.int64, device=dev)
+        b = torch.tensor(dsts, dtype=torch.int64, device=dev)
+        for _ in range(3):
+            pkv.compact_tokens(a, b, kc2, vc2)
+        t = _timed(lambda: pkv.compact_tokens(a, b, kc2, vc2), steps, stream)
+        assert pkv.check_device_error() == 0
+        nbytes = len(srcs) * 2 * wl.num_kv_heads * wl.head_dim * 2 * 2 + 2 * 8 * len(srcs)  # read+write K,V + slots
+        gbs = nbytes / t / 1e6
+        peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+        line = {"metric": "compact_tokens GB/s (token rows moved into fresh target blocks)", "value": gbs,
+                "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": 3, "higher_is_better": True,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": "compact", "tokens": len(srcs), "kept": "every other token of each "
+                           "llama8b sequence"},
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                             "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": t},
+                "gpu_launches": pkv.launch_count() - l0}
+    print(json.dumps(line))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload in ("swap", "compact"):
+        return run_data_movement(args)
     return run_ours(args)
 
 
