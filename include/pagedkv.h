@@ -120,6 +120,20 @@ pkv_status paged_kv_append(const void* k, const void* v, const int64_t* slot_map
 size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                        int32_t max_context_len, int32_t partition_size);
 
+/* How paged_attention_decode divides the work (see paged_attention_plan). */
+enum {
+    PKV_PLAN_SINGLE = 0,       /* one CTA per (sequence, head group): no partials */
+    PKV_PLAN_SPLIT = 1,        /* split-K, merged by the last partition of each row */
+    PKV_PLAN_SPLIT_REDUCE = 2  /* split-K with more than 16 partitions, merged by a second kernel */
+};
+
+/*
+ * The decomposition paged_attention_decode uses for these sizes on the
+ * current device; -1 for invalid sizes.  block_size is the cache's.
+ */
+int32_t paged_attention_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t block_size,
+                             int32_t max_context_len, int32_t partition_size);
+
 /*
  * The split-K partition size (tokens) paged_attention_decode uses for these
  * sizes on the current device: partition_size itself when it is non-zero,

@@ -50,7 +50,8 @@ def _stale(target: Path, deps: list[Path]) -> bool:
 def build_library(force: bool = False, verbose: bool = False) -> Path:
     LIBDIR.mkdir(exist_ok=True)
     out = LIBDIR / "libpagedkv.so"
-    deps = [CSRC / s for s in CUDA_SOURCES] + [CSRC / "pkv_internal.cuh", PKG.parent / "include" / "pagedkv.h"]
+    deps = [CSRC / s for s in CUDA_SOURCES] + [CSRC / "pkv_internal.cuh", CSRC / "decode_common.cuh",
+                                                PKG.parent / "include" / "pagedkv.h"]
     if not force and not _stale(out, deps):
         return out
     nvcc = _nvcc()

@@ -63,6 +63,8 @@ def _lib() -> ctypes.CDLL:
     lib.paged_kv_append.restype = ctypes.c_int
     lib.paged_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.paged_attention_workspace_bytes.restype = sz
+    lib.paged_attention_plan.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.paged_attention_plan.restype = i32
     lib.paged_attention_partition_size.argtypes = [i32, i32, i32, i32, i32]
     lib.paged_attention_partition_size.restype = i32
     lib.paged_attention_decode.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp, i32,
@@ -145,6 +147,17 @@ def paged_attention_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: i
                                     partition_size: int = 0) -> int:
     return int(_lib().paged_attention_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
                                                       partition_size))
+
+
+PLAN_NAMES = {0: "single", 1: "split", 2: "split+reduce"}
+
+
+def paged_attention_plan(num_seqs: int, num_q_heads: int, num_kv_heads: int, block_size: int, max_context_len: int,
+                         partition_size: int = 0) -> str:
+    """Decomposition a decode call with these sizes uses on the current device."""
+    k = int(_lib().paged_attention_plan(num_seqs, num_q_heads, num_kv_heads, block_size, max_context_len,
+                                        partition_size))
+    return PLAN_NAMES.get(k, "invalid")
 
 
 def paged_attention_partition_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, max_context_len: int,

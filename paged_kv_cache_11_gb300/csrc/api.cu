@@ -66,19 +66,18 @@ static pkv_status encode_cache_map(CUtensorMap* m, const void* base, const pkv_c
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_INVALID_ARG;
 }
 
-// Workspace of a split-K call: the fused merge's arrival counters (one per
-// sequence and query head, an upper bound on the head groups), then the
-// partial outputs [B][Hq][parts][D] and log-sum-exps [B][Hq][parts], each
-// region 256-byte aligned.
+// Workspace of a split-K call: first the arrival counters of the in-kernel
+// merge (one per sequence and query head, an upper bound on the head groups),
+// then the partial outputs [B][Hq][parts][D] and log-sum-exps [B][Hq][parts],
+// each region 256-byte aligned.
 struct WorkspaceLayout {
     int64_t ctr_off, o_off, lse_off, total;
 };
 
 static int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
-static WorkspaceLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim, int64_t parts) {
+static WorkspaceLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim, int64_t rows) {
     WorkspaceLayout w;
-    const int64_t rows = num_seqs * num_q_heads * parts;
     w.ctr_off = 0;
     w.o_off = round256(num_seqs * num_q_heads * 8);
     w.lse_off = w.o_off + round256(rows * head_dim * 4);
@@ -134,6 +133,27 @@ static int resolve_partition(int32_t partition_size, int64_t rows, int32_t max_c
         if (units >= 2 * slots) best = P;
     }
     return best;
+}
+
+
+// How a decode call divides its work (see paged_attention_plan).
+struct Plan {
+    int kind;        // PKV_PLAN_*
+    int partition;   // split-K partition (tokens)
+    int max_parts;   // split-K partitions of the longest sequence
+};
+
+static Plan make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t head_tiles, int32_t max_context_len,
+                      int32_t partition_size) {
+    Plan pl;
+    const int64_t groups = (int64_t)num_seqs * num_kv_heads * head_tiles;  // (sequence, head group) rows
+    pl.partition = resolve_partition(partition_size, groups, max_context_len);
+    pl.max_parts = max_context_len == 0 ? 1 : (max_context_len + pl.partition - 1) / pl.partition;
+    if (pl.max_parts <= 1)
+        pl.kind = PKV_PLAN_SINGLE;
+    else
+        pl.kind = pl.max_parts <= kFuseMergeMaxParts ? PKV_PLAN_SPLIT : PKV_PLAN_SPLIT_REDUCE;
+    return pl;
 }
 
 }  // namespace pkv
@@ -198,8 +218,19 @@ size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, in
     const int64_t P = partition_size == 0 ? kAutoPartition : partition_size;  // auto never goes below 512
     const int64_t parts = max_context_len == 0 ? 1 : (max_context_len + P - 1) / P;
     if (parts <= 1) return 0;
-    const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, head_dim, parts);
+    const int64_t rows = (int64_t)num_seqs * num_q_heads * parts;
+    const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, head_dim, rows);
     return (size_t)w.total;
+}
+
+int32_t paged_attention_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t block_size,
+                             int32_t max_context_len, int32_t partition_size) {
+    if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 ||
+        max_context_len < 0 || partition_size < 0 || block_size < 1)
+        return -1;
+    const int group = num_q_heads / num_kv_heads;
+    const int head_tiles = (group + decode_head_tile(group) - 1) / decode_head_tile(group);
+    return make_plan(num_seqs, num_kv_heads, head_tiles, max_context_len, partition_size).kind;
 }
 
 int32_t paged_attention_partition_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
@@ -251,13 +282,13 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
                          !aligned(slot_mapping, 8)))
         return PKV_ERR_INVALID_ARG;
 
-    const int P = resolve_partition(partition_size, (int64_t)num_seqs * cache->num_kv_heads * head_tiles,
-                                    max_context_len);
-    const int max_parts = max_context_len == 0 ? 1 : (max_context_len + P - 1) / P;
-    const bool split = max_parts > 1;
     const size_t need = paged_attention_workspace_bytes(num_seqs, num_q_heads, kHeadDim, max_context_len,
                                                         partition_size);
-    if (split && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return PKV_ERR_WORKSPACE;
+    const bool have_ws = need > 0 && workspace && workspace_bytes >= need && aligned(workspace, 256);
+    const Plan pl = make_plan(num_seqs, cache->num_kv_heads, head_tiles, max_context_len, partition_size);
+    const int P = pl.partition, max_parts = pl.max_parts;
+    const bool split = pl.kind != PKV_PLAN_SINGLE;
+    if (split && !have_ws) return PKV_ERR_WORKSPACE;
 
     int* err = error_word();
     if (!err) return PKV_ERR_CUDA;
@@ -274,7 +305,8 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
     p.context_lens = context_lens;
     p.out = out;
     if (split) {
-        const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, kHeadDim, max_parts);
+        const int64_t rows = (int64_t)num_seqs * num_q_heads * max_parts;
+        const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, kHeadDim, rows);
         char* base = static_cast<char*>(workspace);
         p.merge_ctr = reinterpret_cast<unsigned long long*>(base + w.ctr_off);
         p.part_o = reinterpret_cast<float*>(base + w.o_off);

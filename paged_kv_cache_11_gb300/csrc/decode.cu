@@ -36,7 +36,7 @@
 // columns; it lands as two [BS][64] halves, 128 bytes per row, with the TMA
 // 128-byte swizzle (16-byte chunk c of row r stored at chunk c ^ (r & 7)),
 // which makes the ldmatrix row gathers below bank-conflict free.
-#include "pkv_internal.cuh"
+#include "decode_common.cuh"
 
 namespace pkv {
 
@@ -46,7 +46,6 @@ struct DecodeSmem {
     static constexpr int kHalfBytes = kTileBytes / 2;     // its 64-column half
     static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
     static constexpr int kStagesBytes = NST * kStageBytes;
-    static constexpr int kRedStride = kHeadDim + 4;       // floats per merged row
     static constexpr int kRedBytes = NCW * HT * kRedStride * 4 + NCW * HT * 2 * 4;
     // the merge buffer reuses the ring once every stage has been consumed
     static constexpr int kRingBytes = ((kStagesBytes > kRedBytes ? kStagesBytes : kRedBytes) + 1023) / 1024 * 1024;
@@ -55,34 +54,6 @@ struct DecodeSmem {
     static constexpr int kTotal = kFlagOffset + 16;  // flags[0]: errors, flags[1]: last-arrival verdict
     static constexpr int kDynamic = kTotal + 1024;        // slack to align the base to 1024 B
 };
-
-__device__ __forceinline__ void store_out(const DecodeParams& p, int s, int h, int d, float v) {
-    const int64_t i = ((int64_t)s * p.num_q_heads + h) * kHeadDim + d;
-    if (p.out_dtype == PKV_FP32)
-        static_cast<float*>(p.out)[i] = v;
-    else if (p.out_dtype == PKV_BF16)
-        static_cast<__nv_bfloat16*>(p.out)[i] = __float2bfloat16_rn(v);
-    else
-        static_cast<__half*>(p.out)[i] = __float2half_rn(v);
-}
-
-// Count one arrival of this call (epoch) on a (epoch << 16 | count) counter
-// and report whether it was the nparts-th.  A counter left by another call
-// (different epoch) counts as zero, so stale or garbage contents never
-// matter; the last arrival also resets the count, so a replay of the same
-// launch (same epoch, e.g. from a captured graph) starts from zero too.
-// Lock-free: a failed CAS means another CTA's arrival got in first, so the
-// loop ends after at most nparts tries.
-__device__ __forceinline__ bool arrive_last(unsigned long long* ctr, unsigned long long epoch, int nparts) {
-    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
-    for (;;) {
-        const unsigned long long cnt = (old >> 16) == epoch ? (old & 0xFFFFull) + 1 : 1;
-        const bool last = cnt == (unsigned long long)nparts;
-        const unsigned long long prev = atomicCAS(ctr, old, (epoch << 16) | (last ? 0ull : cnt));
-        if (prev == old) return last;
-        old = prev;
-    }
-}
 
 // Merge the nparts partial (o_p, lse_p) of query heads h0 .. h0+rows-1 of
 // sequence s into out: out = sum_p 2^(lse_p - LSE) o_p, LSE = log2 sum_p
@@ -141,22 +112,6 @@ __device__ __noinline__ void merge_row_partials(const DecodeParams& p, int s, in
     }
 }
 
-// Tunables (compile-time): consumer warps per CTA, ring stages for 16- and
-// 32-token blocks, and the minimum resident CTAs per SM the register
-// allocation must allow.
-#ifndef PKV_NCW
-#define PKV_NCW 2
-#endif
-#ifndef PKV_NST16
-#define PKV_NST16 4
-#endif
-#ifndef PKV_NST32
-#define PKV_NST32 2
-#endif
-#ifndef PKV_MINB
-#define PKV_MINB kDecodeCtasPerSm
-#endif
-
 // NH: 8-head n-tiles per CTA (1: up to 8 query heads of a group, 2: up to 16).
 template <bool kBF16, int BS, int NH, int NCW, int NST>
 __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB - 1)
@@ -165,7 +120,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
     using S = DecodeSmem<BS, NCW, NST, 8 * NH>;
     constexpr int D = kHeadDim;
     constexpr int HT = 8 * NH;     // query heads per CTA
-    constexpr int kSub = BS / 16;  // 16-token sub-blocks per block
     static_assert(BS % 16 == 0, "block size must be a multiple of 16");
     static_assert(NST % NCW == 0, "each ring stage must belong to one consumer warp");
 
@@ -225,18 +179,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
     }
     __syncthreads();
 
-    // Consumer state.  The contraction is written transposed: S^T = K Q^T with
-    // the 16 tokens of a sub-block as the MMA M dimension and the query heads
-    // as N (8 per n-tile), and O^T = V^T P^T with head_dim as M.  Thread
-    // (g = lane/4, t = lane%4) owns heads 8n + 2t, 8n + 2t + 1 of every tile.
-    float acc[8][NH][4];  // O^T: m-tile (16 dims) x n-tile x fragment
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int n = 0; n < NH; ++n) acc[mt][n][0] = acc[mt][n][1] = acc[mt][n][2] = acc[mt][n][3] = 0.f;
-    float mrun[NH][2], lrun[NH][2];
-#pragma unroll
-    for (int n = 0; n < NH; ++n) mrun[n][0] = mrun[n][1] = -INFINITY, lrun[n][0] = lrun[n][1] = 0.f;
+    WarpAcc<NH> acc;  // consumer state (registers); see decode_common.cuh
+    acc_reset(acc);
     int issued = 0;  // producer lane 0: TMA stages issued
 
     if (warp == NCW) {
@@ -307,26 +251,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
         }
     } else {
         // ------------------------------------------------------------ consumers
-        const int g = lane >> 2, t = lane & 3;
-        // Q^T as the B operand of S^T = K Q^T: for k-step ks, b0 holds
-        // q[head][16 ks + 2t .. +1], b1 holds q[head][16 ks + 8 + 2t .. +1].
-        uint32_t qb[NH][8][2];
-#pragma unroll
-        for (int n = 0; n < NH; ++n) {
-            const int hr = 8 * n + g;
-            const uint32_t* qr = hr < rows ? reinterpret_cast<const uint32_t*>(
-                                                 static_cast<const uint16_t*>(p.q) +
-                                                 ((int64_t)s * p.num_q_heads + h0 + hr) * D)
-                                           : nullptr;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                qb[n][ks][0] = qr ? __ldg(qr + 8 * ks + t) : 0u;
-                qb[n][ks][1] = qr ? __ldg(qr + 8 * ks + 4 + t) : 0u;
-            }
-        }
+        QFrag<NH> qf;
+        load_q_frag(qf, p, s, h0, rows, lane);
         const float sl2 = p.scale_log2;
-        const int mi = lane >> 3, rr = lane & 7;
-
         for (int jj = warp; jj < nblk; jj += NCW) {
             const int st = jj % NST, round = jj / NST;
             // every lane waits (each needs the acquire of the TMA writes); the
@@ -340,119 +267,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
             }
             const int valid = min(BS, tok1 - (tok0 + jj * BS));  // >= 1
             const uint32_t kb = smem_addr(stages + st * S::kStageBytes);
-            const uint32_t vb = kb + S::kTileBytes;
-
-#pragma unroll
-            for (int sub = 0; sub < kSub; ++sub) {
-                if (sub * 16 >= valid) break;  // warp-uniform: nothing valid left in this block
-                // ---- S^T = K Q^T for tokens sub*16 .. sub*16+15 (M) x heads (N)
-                float sc[NH][4];
-#pragma unroll
-                for (int n = 0; n < NH; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-                {
-                    // A = K rows: matrices (tokens 0-7 | 8-15) x (dims lo | hi of the k-step)
-                    const int tok = sub * 16 + (mi & 1) * 8 + rr;
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const int chunk = 2 * ks + (mi >> 1);
-                        const int line = (chunk >> 3) * BS + tok;
-                        const uint32_t addr = kb + line * 128 + (((chunk & 7) ^ rr) << 4);
-                        uint32_t a[4];
-                        ldsm_x4(addr, a[0], a[1], a[2], a[3]);
-#pragma unroll
-                        for (int n = 0; n < NH; ++n) mma_16816<kBF16>(sc[n], a, qb[n][ks][0], qb[n][ks][1]);
-                    }
-                }
-                // ---- scale (log2 domain), mask past the context, online softmax per head
-                const int ta = sub * 16 + g, tb = ta + 8;  // tokens of sc[.][0..1] and sc[.][2..3]
-                const bool va = ta < valid, vb_ = tb < valid;
-                uint32_t ph[NH][2], pl[NH][2];
-#pragma unroll
-                for (int n = 0; n < NH; ++n) {
-                    sc[n][0] = va ? sc[n][0] * sl2 : -INFINITY;
-                    sc[n][1] = va ? sc[n][1] * sl2 : -INFINITY;
-                    sc[n][2] = vb_ ? sc[n][2] * sl2 : -INFINITY;
-                    sc[n][3] = vb_ ? sc[n][3] * sl2 : -INFINITY;
-                    float mx0 = fmaxf(sc[n][0], sc[n][2]), mx1 = fmaxf(sc[n][1], sc[n][3]);
-#pragma unroll
-                    for (int o = 4; o < 32; o <<= 1) {
-                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-                    }
-                    const float mn0 = fmaxf(mrun[n][0], mx0), mn1 = fmaxf(mrun[n][1], mx1);
-                    const float al0 = mn0 == -INFINITY ? 1.f : exp2f(mrun[n][0] - mn0);
-                    const float al1 = mn1 == -INFINITY ? 1.f : exp2f(mrun[n][1] - mn1);
-                    const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
-                    const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-                    mrun[n][0] = mn0;
-                    mrun[n][1] = mn1;
-                    const float p0 = exp2f(sc[n][0] - ms0), p1 = exp2f(sc[n][1] - ms1);
-                    const float p2 = exp2f(sc[n][2] - ms0), p3 = exp2f(sc[n][3] - ms1);
-                    lrun[n][0] = lrun[n][0] * al0 + (p0 + p2);
-                    lrun[n][1] = lrun[n][1] * al1 + (p1 + p3);
-#pragma unroll
-                    for (int mt = 0; mt < 8; ++mt) {
-                        acc[mt][n][0] *= al0;
-                        acc[mt][n][1] *= al1;
-                        acc[mt][n][2] *= al0;
-                        acc[mt][n][3] *= al1;
-                    }
-                    // P^T rows (tokens) x columns (heads) in the accumulator
-                    // layout; movmatrix.trans turns each 8x8 half into the B
-                    // operand layout of O^T = V^T P^T.  High part + residual.
-                    float r0, r1, r2, r3;
-                    const uint32_t h01 = pack2<kBF16>(p0, p1, r0, r1);
-                    const uint32_t h23 = pack2<kBF16>(p2, p3, r2, r3);
-                    const uint32_t l01 = pack2<kBF16>(p0 - r0, p1 - r1);
-                    const uint32_t l23 = pack2<kBF16>(p2 - r2, p3 - r3);
-                    ph[n][0] = movmatrix_trans(h01);
-                    ph[n][1] = movmatrix_trans(h23);
-                    pl[n][0] = movmatrix_trans(l01);
-                    pl[n][1] = movmatrix_trans(l23);
-                }
-                // ---- O^T += V^T P^T over the 16 tokens
-                {
-                    // A = V^T: matrices (tokens 0-7 | 8-15) x (dims 16mt+0..7 | +8..15), transposed
-                    const int tok = sub * 16 + (mi >> 1) * 8 + rr;
-                    const bool tail = sub * 16 + 16 > valid;
-                    // V rows past the context may hold anything (even NaN): zero them
-                    // in the A fragments rather than rely on p == 0.
-                    const int tt = sub * 16 + 2 * t;
-                    const uint32_t keep0 = (tt < valid ? 0x0000ffffu : 0u) | (tt + 1 < valid ? 0xffff0000u : 0u);
-                    const uint32_t keep1 =
-                        (tt + 8 < valid ? 0x0000ffffu : 0u) | (tt + 9 < valid ? 0xffff0000u : 0u);
-#pragma unroll
-                    for (int mt = 0; mt < 8; ++mt) {
-                        const int chunk = 2 * mt + (mi & 1);
-                        const int line = (chunk >> 3) * BS + tok;
-                        const uint32_t addr = vb + line * 128 + (((chunk & 7) ^ rr) << 4);
-                        uint32_t a[4];
-                        ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
-                        if (tail) {
-                            a[0] &= keep0;
-                            a[1] &= keep0;
-                            a[2] &= keep1;
-                            a[3] &= keep1;
-                        }
-#pragma unroll
-                        for (int n = 0; n < NH; ++n) {
-                            mma_16816<kBF16>(acc[mt][n], a, ph[n][0], ph[n][1]);
-                            mma_16816<kBF16>(acc[mt][n], a, pl[n][0], pl[n][1]);
-                        }
-                    }
-                }
-            }
+            attend_block<kBF16, BS, NH>(acc, qf, kb, kb + S::kTileBytes, valid, sl2, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
         }
-        // full per-head sums: the eight lanes g = 0..7 hold disjoint tokens
-#pragma unroll
-        for (int n = 0; n < NH; ++n)
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                lrun[n][0] += __shfl_xor_sync(0xffffffffu, lrun[n][0], o);
-                lrun[n][1] += __shfl_xor_sync(0xffffffffu, lrun[n][1], o);
-            }
+        acc_finish(acc);
     }
     __syncthreads();
 
@@ -468,65 +287,24 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
     __syncthreads();
 
     // ---- merge the per-warp states (stage memory is free now)
-    float* red = reinterpret_cast<float*>(smem);          // [NCW][HT][kRedStride]
-    float* ml = red + NCW * HT * S::kRedStride;            // [NCW][HT][2]
-    if (warp < NCW) {
-        const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-        for (int n = 0; n < NH; ++n) {
-            const int ha = 8 * n + 2 * t, hb = ha + 1;
-            float* ra = red + (warp * HT + ha) * S::kRedStride;
-            float* rb = red + (warp * HT + hb) * S::kRedStride;
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                const int d0 = 16 * mt + g;
-                if (ha < rows) {
-                    ra[d0] = acc[mt][n][0];
-                    ra[d0 + 8] = acc[mt][n][2];
-                }
-                if (hb < rows) {
-                    rb[d0] = acc[mt][n][1];
-                    rb[d0 + 8] = acc[mt][n][3];
-                }
-            }
-            if (g == 0) {
-                if (ha < rows) {
-                    ml[(warp * HT + ha) * 2] = mrun[n][0];
-                    ml[(warp * HT + ha) * 2 + 1] = lrun[n][0];
-                }
-                if (hb < rows) {
-                    ml[(warp * HT + hb) * 2] = mrun[n][1];
-                    ml[(warp * HT + hb) * 2 + 1] = lrun[n][1];
-                }
-            }
-        }
-    }
+    float* red = reinterpret_cast<float*>(smem);      // [NCW][HT][kRedStride]
+    float* ml = red + NCW * HT * kRedStride;           // [NCW][HT][2]
+    if (warp < NCW) acc_to_smem(acc, red, ml, warp, rows, lane);
     __syncthreads();
 
     const bool bad = fl != 0;
     for (int i = tid; i < rows * D; i += blockDim.x) {
         const int hr = i / D, d = i % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) M = fmaxf(M, ml[(w * HT + hr) * 2]);
-        float lsum = 0.f, o = 0.f;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) {
-            const float mw = ml[(w * HT + hr) * 2];
-            if (mw != -INFINITY) {
-                const float f = exp2f(mw - M);
-                lsum += f * ml[(w * HT + hr) * 2 + 1];
-                o += f * red[(w * HT + hr) * S::kRedStride + d];
-            }
-        }
+        float lse;
+        const float o = combine_warps<NCW, HT>(red, ml, hr, d, lse);
         const int h = h0 + hr;
         if (write_partial) {
             const int64_t idx = ((int64_t)s * p.num_q_heads + h) * p.max_parts + part;
-            p.part_o[idx * D + d] = bad ? 0.f : o / lsum;
+            p.part_o[idx * D + d] = bad ? 0.f : o;
             // +inf marks a partition whose metadata was bad: the merge zeroes the output.
-            if (d == 0) p.part_lse[idx] = bad ? INFINITY : M + log2f(lsum);
+            if (d == 0) p.part_lse[idx] = bad ? INFINITY : lse;
         } else {
-            store_out(p, s, h, d, bad ? 0.f : o / lsum);
+            store_out(p, s, h, d, bad ? 0.f : o);
         }
     }
 

@@ -27,7 +27,8 @@ def test_header_declares_the_entry_points():
     names = set(declared_functions())
     assert {"paged_kv_append", "paged_attention_decode", "copy_blocks", "paged_attention_workspace_bytes",
             "pkv_check_device_error", "pkv_status_string", "pkv_launch_count", "pkv_version",
-            "paged_attention_partition_size"} <= names
+            "paged_attention_partition_size", "paged_attention_plan", "paged_attention_append_decode",
+            "swap_blocks", "compact_tokens"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -72,6 +73,14 @@ def test_decode_host_validation(lib):
     assert _decode(lib, d, ptr=18) == binding.PKV_ERR_INVALID_ARG             # misaligned pointers
     assert _decode(lib, d, max_ctx=64, P=16) == binding.PKV_ERR_WORKSPACE     # split needs a workspace
     assert _decode(lib, d, num_seqs=70000) == binding.PKV_ERR_INVALID_ARG
+
+
+def test_plan_query(lib):
+    assert binding.paged_attention_plan(8, 64, 8, 32, 131072, 0) == "split+reduce"   # long contexts
+    assert binding.paged_attention_plan(4, 4, 1, 16, 100, 0) == "single"             # few rows, short
+    assert binding.paged_attention_plan(64, 32, 8, 16, 4096, 0) == "split"
+    assert binding.paged_attention_plan(64, 32, 8, 16, 4096, 4096) == "single"       # explicit partition
+    assert binding.paged_attention_plan(8, 64, 7, 16, 100, 0) == "invalid"
 
 
 def test_partition_size_query(lib):
