@@ -298,3 +298,40 @@ def test_full_size_sampled(gpu, name, nsample):
     assert err <= TOL, err
     o = out.float()
     assert torch.isfinite(o).all()
+
+
+# ------------------------------------------------------------------ graph capture
+@pytest.mark.parametrize("P", [0, 64])  # merge in the decode kernel / merge kernel
+def test_decode_step_captured_in_a_cuda_graph(gpu, P):
+    """A fused decode step captured once and replayed: each replay gives the direct call's bits
+    (the split-K arrival counters are reset by their last arrival, so a replayed epoch starts clean)."""
+    import paged_kv_cache_11_gb300 as pkv
+    wl = W.make_workload("llama8b", num_seqs=16, lens=("uniform", 300, 2000), seed=12)
+    dev = gpu
+    kc, vc, q = to_dev(wl.k_cache, "bf16", dev), to_dev(wl.v_cache, "bf16", dev), to_dev(wl.q, "bf16", dev)
+    nk, nv = to_dev(wl.new_k, "bf16", dev), to_dev(wl.new_v, "bf16", dev)
+    sm = torch.from_numpy(wl.slot_mapping).to(dev)
+    bt, cl = torch.from_numpy(wl.block_tables).to(dev), torch.from_numpy(wl.context_lens).to(dev)
+    mcl = wl.max_context_len
+    need = pkv.paged_attention_workspace_bytes(wl.num_seqs, wl.num_q_heads, 128, mcl, P)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty((wl.num_seqs, wl.num_q_heads, 128), device=dev)
+    step = lambda: pkv.paged_attention_append_decode(q, nk, nv, sm, kc, vc, bt, cl, wl.scale, out=out,
+                                                     max_context_len=mcl, partition_size=P, workspace=ws)
+    step()
+    torch.cuda.synchronize()
+    ref = out.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()                                   # warm the stream before capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(5):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    assert pkv.check_device_error() == 0
