@@ -53,6 +53,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seqs", type=int, default=0, help="0: the whole batch")
     ap.add_argument("--unfused", action="store_true", help="separate block-write and decode launches")
+    ap.add_argument("--ungrouped", action="store_true",
+                    help="shared-prefix workloads: plain paged_attention_decode instead of the grouped call")
     return ap.parse_args(argv)
 
 
@@ -107,14 +109,21 @@ def measured_peaks() -> dict:
     return {}
 
 
+def decode_source_hash() -> str:
+    """sha256[:16] over the sources the decode kernels are built from."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("decode.cu", "group_prefix.cu", "decode_common.cuh", "pkv_internal.cuh"):
+        h.update((ROOT / "paged_kv_cache_11_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
 def traffic_per_launch(workload: str):
-    """dram read+write bytes per decode launch from the committed ncu summary, if it
-    still describes the current kernel (same source hash)."""
+    """dram read+write bytes per decode call from the committed ncu summary, if it
+    still describes the current kernels (same source hash)."""
     if not TRAFFIC_FILE.exists():
         return None
-    import hashlib
-    src = (ROOT / "paged_kv_cache_11_gb300" / "csrc" / "decode.cu").read_bytes()
-    h = hashlib.sha256(src).hexdigest()[:16]
+    h = decode_source_hash()
     for line in TRAFFIC_FILE.read_text().splitlines():
         parts = line.split()
         if len(parts) >= 3 and parts[0] == workload and parts[1] == h:
@@ -200,10 +209,13 @@ def describe(wl) -> dict:
     return d
 
 
-def decode_algorithmic_bytes(wl, fused: bool = False) -> int:
+def decode_algorithmic_bytes(wl, fused: bool = False, groups=None) -> int:
     """Bytes paged_attention_decode must move: the attended K/V, q, the block-table
     entries it reads, context_lens and the fp32 output; the fused call also reads
-    each new K/V row and its slot and writes the row into the cache."""
+    each new K/V row and its slot and writes the row into the cache.  The grouped
+    call (groups = (group_starts, prefix_lens)) must read each shared block once:
+    the distinct K/V slots, plus each group's shared table entries once, the
+    prefix lengths and the group starts."""
     bs = wl.block_size
     blocks = int(((wl.context_lens.astype(np.int64) + bs - 1) // bs).sum())
     q = wl.num_seqs * wl.num_q_heads * wl.head_dim * 2
@@ -211,6 +223,10 @@ def decode_algorithmic_bytes(wl, fused: bool = False) -> int:
     extra = 0
     if fused:
         extra = wl.num_seqs * (2 * 2 * wl.num_kv_heads * wl.head_dim * 2 + 8)
+    if groups is not None:
+        gs, pl = groups
+        shared = int(pl.sum()) // bs - sum(int(pl[a]) // bs for a in gs[:-1] if a < len(pl))
+        return wl.unique_kv_bytes() + q + out + (blocks - shared) * 4 + wl.num_seqs * 8 + len(gs) * 4
     return wl.kv_bytes() + q + out + blocks * 4 + wl.num_seqs * 4 + extra
 
 
@@ -311,14 +327,33 @@ def run_ours(args):
     cow = torch.from_numpy(wl.cow_pairs).to(dev) if len(wl.cow_pairs) else None
     out = torch.empty((wl.num_seqs, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
     mcl = wl.max_context_len
-    need = pkv.paged_attention_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, mcl, args.partition_size)
-    wsp = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     # A decode step that appends one token per sequence, at its last position,
     # runs as one fused launch (block write + attention); other steps (the
-    # shared-prefix continuation) run copy_blocks, paged_kv_append, decode.
+    # shared-prefix continuation) run copy_blocks, paged_kv_append, decode --
+    # the grouped decode when the batch holds forked groups.
     fused = (not args.unfused) and cow is None and np.array_equal(wl.append_seq, np.arange(wl.num_seqs))
+    grouped = bool(spec.groups) and not args.ungrouped and not fused
+    if grouped:
+        g_starts, g_plen, g_max = W.prefix_groups(wl)
+        g_mpl = int(g_plen.max())
+        gs_d, pl_d = torch.from_numpy(g_starts).to(dev), torch.from_numpy(g_plen).to(dev)
+        need = pkv.paged_attention_grouped_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, mcl, g_mpl,
+                                                           args.partition_size)
+    else:
+        need = pkv.paged_attention_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, mcl,
+                                                   args.partition_size)
+    wsp = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+
+    def decode(q_, bt_, cl_, out_, ws_, gs_=None, pl_=None):
+        if grouped:
+            pkv.paged_attention_decode_grouped(q_, kc, vc, bt_, cl_, gs_, pl_, wl.scale, max_group_size=g_max,
+                                               max_prefix_len=g_mpl, out=out_, max_context_len=mcl,
+                                               partition_size=args.partition_size, workspace=ws_)
+        else:
+            pkv.paged_attention_decode(q_, kc, vc, bt_, cl_, wl.scale, out=out_, max_context_len=mcl,
+                                       partition_size=args.partition_size, workspace=ws_)
 
     def step(ev=None):
         if ev is not None:
@@ -333,8 +368,7 @@ def run_ours(args):
                 pkv.paged_kv_append(nk, nv, sm, kc, vc)
             if ev is not None:
                 ev[0].record(stream)
-            pkv.paged_attention_decode(q, kc, vc, bt, cl, wl.scale, out=out, max_context_len=mcl,
-                                       partition_size=args.partition_size, workspace=wsp)
+            decode(q, bt, cl, out, wsp, gs_d if grouped else None, pl_d if grouped else None)
         if ev is not None:
             ev[1].record(stream)
 
@@ -381,6 +415,8 @@ def run_ours(args):
                   ("cl", wl.context_lens, torch.int32)]
     if cow is not None:
         host_parts.append(("cow", wl.cow_pairs, torch.int64))
+    if grouped:
+        host_parts += [("gs", g_starts, torch.int32), ("pl", g_plen, torch.int32)]
     offs, off = {}, 0
     for name, arr, _ in host_parts:
         offs[name] = off
@@ -427,9 +463,7 @@ def run_ours(args):
                     pkv.copy_blocks(kc, vc, v["cow"])
                 if len(wl.slot_mapping):
                     pkv.paged_kv_append(v["nk"], v["nv"], v["sm"], kc, vc)
-                pkv.paged_attention_decode(v["q"], kc, vc, v["bt"], v["cl"], wl.scale, out=d_out[b],
-                                           max_context_len=mcl, partition_size=args.partition_size,
-                                           workspace=wsp2[b])
+                decode(v["q"], v["bt"], v["cl"], d_out[b], wsp2[b], v.get("gs"), v.get("pl"))
             comp_done[b].record(cs)
 
     def d2h_copy(i):
@@ -482,9 +516,11 @@ def run_ours(args):
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     steps = args.steps
     value = kv_all * steps / (ms_max / 1e3) / 1e9
-    dec_bytes = decode_algorithmic_bytes(wl, fused)
+    dec_bytes = decode_algorithmic_bytes(wl, fused, (g_starts, g_plen) if grouped else None)
     achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
-    traffic = traffic_per_launch(args.workload)
+    traffic = traffic_per_launch(args.workload + ("_grouped" if grouped else ""))
+    dec_api = ("paged_attention_append_decode" if fused else
+               "paged_attention_decode_grouped" if grouped else "paged_attention_decode")
 
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
@@ -503,14 +539,14 @@ def run_ours(args):
         "dtype": wl.dtype, "data": "synthetic",
         "config": {**describe(wl), "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": f"inputs larger than L2 ({wl.kv_bytes() / 1e6:.0f} MB of K/V vs 129 MB), no flush",
-                   "api": "paged_attention_append_decode" if fused else
-                          "copy_blocks + paged_kv_append + paged_attention_decode",
+                   "api": dec_api if fused else "copy_blocks + paged_kv_append + " + dec_api,
                    "partition_size": pkv.paged_attention_partition_size(
                        wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, mcl, args.partition_size)},
         "seq_per_s": seqs_all * steps / (ms_max / 1e3),
         "pct_of_hbm_peak": 100.0 * value / peak,
-        "roofline": {"kernel": ("paged_attention_append_decode" if fused else "paged_attention_decode")
-                     + " (decode kernel + split-K merge)", "bound": "hbm",
+        "roofline": {"kernel": dec_api + (" (shared-prefix kernel + decode kernel + merge; bytes: each distinct "
+                                          "K/V slot once)" if grouped else " (decode kernel + split-K merge)"),
+                     "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src, "traffic": traffic,
                      "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_avg_ms},

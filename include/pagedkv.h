@@ -76,7 +76,11 @@ enum {
     PKV_DEVERR_COPY_ID = 2,     /* copy_blocks / swap_blocks: src or dst outside its pool */
     PKV_DEVERR_CONTEXT_LEN = 3, /* decode: context_lens[s] < 0, above the table's capacity, or above max_context_len */
     PKV_DEVERR_BLOCK_ID = 4,    /* decode: block_tables entry outside the pool */
-    PKV_DEVERR_TIMEOUT = 5      /* a bounded in-CTA wait ran out */
+    PKV_DEVERR_TIMEOUT = 5,     /* a bounded in-CTA wait ran out */
+    PKV_DEVERR_PREFIX_LEN = 6,  /* grouped decode: prefix_lens[s] < 0, above context_lens[s] or
+                                   max_prefix_len, or not a multiple of block_size */
+    PKV_DEVERR_GROUP = 7        /* grouped decode: group_starts out of order or range, or a sequence
+                                   with a shared prefix in no group or in two */
 };
 
 /* Shape of one layer's paged cache (host struct, read during the call). */
@@ -214,6 +218,60 @@ pkv_status paged_attention_append_decode(const void* q, const void* k_new, const
                                          int32_t max_context_len, float scale, void* out, int32_t out_dtype,
                                          const pkv_cache_desc* cache, int32_t partition_size, void* workspace,
                                          size_t workspace_bytes, void* stream);
+
+/*
+ * paged_attention_decode for batches whose sequences share prompt blocks
+ * (samples forked from one prompt, a common system prompt).  Forked
+ * sequences map the prompt's logical blocks to the same physical blocks,
+ * counted by reference ("vllm", "como funciona"; techtrendfeed "KV Cache
+ * Administration", "How PagedAttention Works", step 4), and a shared prefix
+ * is read once and reused (aitalk.it "PagedAttention e RadixAttention").
+ * Here each shared block is read from HBM once per (group, KV head) and
+ * attended by every member's query heads together; each member's own
+ * blocks are attended as in paged_attention_decode, and the two parts are
+ * merged through their log-sum-exp.
+ *
+ * The result is paged_attention_decode's on the same q, cache, tables and
+ * lengths, provided that for every member s of group g, positions
+ * 0 .. prefix_lens[s]-1 of s sit in the same physical blocks as the same
+ * positions of the group's first member (block_tables rows agree there).
+ *
+ * group_starts:   [num_groups + 1] int32 device memory: the members of group
+ *                 g are sequences group_starts[g] .. group_starts[g+1]-1, in
+ *                 order; groups must not overlap.
+ * max_group_size: host-side upper bound of group_starts[g+1] - group_starts[g].
+ * prefix_lens:    [num_seqs] int32 device memory: tokens of s attended through
+ *                 its group's first member's block table, a multiple of
+ *                 block_size in [0, min(context_lens[s], max_prefix_len)].
+ *                 Members of one group may differ.  A sequence with
+ *                 prefix_lens[s] == 0 need not be in any group.
+ * max_prefix_len: host-side upper bound of prefix_lens, <= max_context_len.
+ * workspace:      at least paged_attention_grouped_workspace_bytes(...)
+ *                 bytes, 256-byte aligned; always needed.  Contents on entry
+ *                 are ignored.
+ * Other arguments as for paged_attention_decode.  Supported: as for
+ * paged_attention_decode, with num_q_heads / num_kv_heads <= 64 and
+ * num_groups <= 65535.  Bad metadata never faults: a prefix length out of
+ * range (PKV_DEVERR_PREFIX_LEN), or a sequence with a nonzero prefix length
+ * that lies in no group, in two groups or in a group beyond max_group_size
+ * members (PKV_DEVERR_GROUP), zeroes that sequence's output; group_starts
+ * out of order or out of range skip the group (PKV_DEVERR_GROUP).  The
+ * pages describe the sharing, not this kernel: the grouped read is an
+ * addition of this library.
+ */
+pkv_status paged_attention_decode_grouped(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                          int32_t max_context_len, const int32_t* group_starts,
+                                          int32_t num_groups, int32_t max_group_size, const int32_t* prefix_lens,
+                                          int32_t max_prefix_len, float scale, void* out, int32_t out_dtype,
+                                          const pkv_cache_desc* cache, int32_t partition_size, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/* Workspace bytes paged_attention_decode_grouped needs (0 for invalid sizes). */
+size_t paged_attention_grouped_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                               int32_t max_context_len, int32_t max_prefix_len,
+                                               int32_t partition_size);
 
 /*
  * paged_attention_decode without a workspace argument, for callers that

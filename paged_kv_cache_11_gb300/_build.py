@@ -19,7 +19,7 @@ from pathlib import Path
 PKG = Path(__file__).resolve().parent
 CSRC = PKG / "csrc"
 LIBDIR = PKG / "_lib"
-CUDA_SOURCES = ["api.cu", "decode.cu", "append_copy.cu", "noalloc.cu"]
+CUDA_SOURCES = ["api.cu", "decode.cu", "group_prefix.cu", "append_copy.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -70,19 +70,27 @@ static pkv_status encode_cache_map(CUtensorMap* m, const void* base, const pkv_c
 // merge (one per sequence and query head, an upper bound on the head groups),
 // then the partial outputs [B][Hq][parts][D] and log-sum-exps [B][Hq][parts],
 // each region 256-byte aligned.
+// Grouped decode adds one group index per sequence after the counters.
 struct WorkspaceLayout {
-    int64_t ctr_off, o_off, lse_off, total;
+    int64_t ctr_off, group_off, o_off, lse_off, total;
 };
 
 static int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
-static WorkspaceLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim, int64_t rows) {
+static WorkspaceLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim, int64_t rows,
+                                        bool grouped = false) {
     WorkspaceLayout w;
     w.ctr_off = 0;
-    w.o_off = round256(num_seqs * num_q_heads * 8);
+    w.group_off = round256(num_seqs * num_q_heads * 8);
+    w.o_off = w.group_off + (grouped ? round256(num_seqs * 4) : 0);
     w.lse_off = w.o_off + round256(rows * head_dim * 4);
     w.total = w.lse_off + round256(rows * 4);
     return w;
+}
+
+// Prefix partitions of grouped decode for the longest shared prefix.
+static int64_t prefix_parts_of(int64_t max_prefix_len) {
+    return (max_prefix_len + kPrefixPartition - 1) / kPrefixPartition;
 }
 
 // Epoch of a decode call: a process-wide counter, 48 bits, never 0.
@@ -223,6 +231,18 @@ size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, in
     return (size_t)w.total;
 }
 
+size_t paged_attention_grouped_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                               int32_t max_context_len, int32_t max_prefix_len,
+                                               int32_t partition_size) {
+    if (num_seqs < 0 || num_q_heads < 1 || head_dim < 1 || max_context_len < 0 || max_prefix_len < 0 ||
+        max_prefix_len > max_context_len || partition_size < 0)
+        return 0;
+    const int64_t P = partition_size == 0 ? kAutoPartition : partition_size;  // auto never goes below 512
+    const int64_t parts = prefix_parts_of(max_prefix_len) + (max_context_len == 0 ? 1 : (max_context_len + P - 1) / P);
+    const int64_t rows = (int64_t)num_seqs * num_q_heads * parts;
+    return (size_t)workspace_layout(num_seqs, num_q_heads, head_dim, rows, true).total;
+}
+
 int32_t paged_attention_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t block_size,
                              int32_t max_context_len, int32_t partition_size) {
     if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 ||
@@ -245,14 +265,23 @@ int32_t paged_attention_partition_size(int32_t num_seqs, int32_t num_q_heads, in
 
 }  // extern "C"
 
+// Shared-prefix groups of paged_attention_decode_grouped.
+struct GroupArgs {
+    const int32_t* group_starts;
+    int32_t num_groups, max_group_size;
+    const int32_t* prefix_lens;
+    int32_t max_prefix_len;
+};
+
 // paged_attention_decode, optionally with the block write of one new token
-// per sequence fused in (k_new != nullptr).
+// per sequence fused in (k_new != nullptr), or with shared-prefix groups
+// (grp != nullptr).
 static pkv_status decode_impl(const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
                               const void* k_cache, const void* v_cache, const int32_t* block_tables,
                               int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
                               int32_t num_q_heads, int32_t max_context_len, float scale, void* out,
                               int32_t out_dtype, const pkv_cache_desc* cache, int32_t partition_size,
-                              void* workspace, size_t workspace_bytes, void* stream) {
+                              void* workspace, size_t workspace_bytes, void* stream, const GroupArgs* grp = nullptr) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
     if (cache->head_dim != kHeadDim) return PKV_ERR_UNSUPPORTED;
@@ -282,12 +311,29 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
                          !aligned(slot_mapping, 8)))
         return PKV_ERR_INVALID_ARG;
 
-    const size_t need = paged_attention_workspace_bytes(num_seqs, num_q_heads, kHeadDim, max_context_len,
-                                                        partition_size);
+    int members_per_tile = 0, row_tiles = 0, prefix_parts = 0;
+    if (grp) {
+        if (group > kPrefixRows) return PKV_ERR_UNSUPPORTED;
+        if (grp->num_groups < 0 || grp->num_groups > 65535 || grp->max_prefix_len < 0 ||
+            grp->max_prefix_len > max_context_len || (grp->num_groups > 0 && grp->max_group_size < 1))
+            return PKV_ERR_INVALID_ARG;
+        if (!grp->prefix_lens || !aligned(grp->prefix_lens, 4) ||
+            (grp->num_groups > 0 && (!grp->group_starts || !aligned(grp->group_starts, 4))))
+            return PKV_ERR_INVALID_ARG;
+        members_per_tile = kPrefixRows / group;
+        row_tiles = grp->num_groups > 0 ? (grp->max_group_size + members_per_tile - 1) / members_per_tile : 0;
+        if ((int64_t)cache->num_kv_heads * row_tiles > 65535) return PKV_ERR_UNSUPPORTED;
+        prefix_parts = (int)prefix_parts_of(grp->max_prefix_len);
+    }
+    const size_t need = grp ? paged_attention_grouped_workspace_bytes(num_seqs, num_q_heads, kHeadDim,
+                                                                      max_context_len, grp->max_prefix_len,
+                                                                      partition_size)
+                            : paged_attention_workspace_bytes(num_seqs, num_q_heads, kHeadDim, max_context_len,
+                                                              partition_size);
     const bool have_ws = need > 0 && workspace && workspace_bytes >= need && aligned(workspace, 256);
     const Plan pl = make_plan(num_seqs, cache->num_kv_heads, head_tiles, max_context_len, partition_size);
-    const int P = pl.partition, max_parts = pl.max_parts;
-    const bool split = pl.kind != PKV_PLAN_SINGLE;
+    const int P = pl.partition, max_parts = pl.max_parts + prefix_parts;
+    const bool split = grp || pl.kind != PKV_PLAN_SINGLE;
     if (split && !have_ws) return PKV_ERR_WORKSPACE;
 
     int* err = error_word();
@@ -306,13 +352,24 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
     p.out = out;
     if (split) {
         const int64_t rows = (int64_t)num_seqs * num_q_heads * max_parts;
-        const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, kHeadDim, rows);
+        const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, kHeadDim, rows, grp != nullptr);
         char* base = static_cast<char*>(workspace);
         p.merge_ctr = reinterpret_cast<unsigned long long*>(base + w.ctr_off);
         p.part_o = reinterpret_cast<float*>(base + w.o_off);
         p.part_lse = reinterpret_cast<float*>(base + w.lse_off);
         p.fuse_merge = max_parts <= kFuseMergeMaxParts ? 1 : 0;
         p.epoch = next_epoch();
+        if (grp) {
+            p.seq_group = reinterpret_cast<int*>(base + w.group_off);
+            p.prefix_lens = grp->prefix_lens;
+            p.group_starts = grp->group_starts;
+            p.max_prefix_len = grp->max_prefix_len;
+            p.prefix_partition = kPrefixPartition;
+            p.prefix_parts = prefix_parts;
+            p.num_groups = grp->num_groups;
+            p.members_per_tile = members_per_tile;
+            p.row_tiles = row_tiles;
+        }
     }
     p.err = err;
     p.num_blocks = cache->num_blocks;
@@ -327,6 +384,7 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
     p.head_tiles = head_tiles;
     p.out_dtype = out_dtype;
     p.split = split ? 1 : 0;
+    p.block_size = cache->block_size;
     p.scale_log2 = scale * 1.4426950408889634f;
     if (fused_append) {
         p.fused_append = 1;
@@ -337,8 +395,12 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
         p.v_cache = static_cast<uint4*>(const_cast<void*>(v_cache));
     }
     int launches = 0;
-    const cudaError_t e =
-        launch_decode(p, cache->dtype, cache->block_size, tmk, tmv, static_cast<cudaStream_t>(stream), &launches);
+    cudaError_t e = cudaSuccess;
+    if (grp && prefix_parts > 0 && grp->num_groups > 0)
+        e = launch_group_prefix(p, cache->dtype, cache->block_size, tmk, tmv, static_cast<cudaStream_t>(stream),
+                                &launches);
+    if (e == cudaSuccess)
+        e = launch_decode(p, cache->dtype, cache->block_size, tmk, tmv, static_cast<cudaStream_t>(stream), &launches);
     g_launches += launches;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
@@ -414,6 +476,20 @@ pkv_status paged_attention_append_decode(const void* q, const void* k_new, const
     return decode_impl(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, max_blocks_per_seq,
                        context_lens, num_seqs, num_q_heads, max_context_len, scale, out, out_dtype, cache,
                        partition_size, workspace, workspace_bytes, stream);
+}
+
+pkv_status paged_attention_decode_grouped(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                          int32_t max_context_len, const int32_t* group_starts,
+                                          int32_t num_groups, int32_t max_group_size, const int32_t* prefix_lens,
+                                          int32_t max_prefix_len, float scale, void* out, int32_t out_dtype,
+                                          const pkv_cache_desc* cache, int32_t partition_size, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+    const GroupArgs grp{group_starts, num_groups, max_group_size, prefix_lens, max_prefix_len};
+    return decode_impl(q, nullptr, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, num_q_heads, max_context_len, scale, out, out_dtype, cache,
+                       partition_size, workspace, workspace_bytes, stream, &grp);
 }
 
 pkv_status copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,

@@ -51,69 +51,14 @@ struct DecodeSmem {
     static constexpr int kRingBytes = ((kStagesBytes > kRedBytes ? kStagesBytes : kRedBytes) + 1023) / 1024 * 1024;
     static constexpr int kBarOffset = kRingBytes;
     static constexpr int kFlagOffset = kBarOffset + 2 * NST * 8;
-    static constexpr int kTotal = kFlagOffset + 16;  // flags[0]: errors, flags[1]: last-arrival verdict
+    static constexpr int kTotal = kFlagOffset + 16;  // flags[0]: errors, [1]: last-arrival verdict, [2]: no group
     static constexpr int kDynamic = kTotal + 1024;        // slack to align the base to 1024 B
 };
 
-// Merge the nparts partial (o_p, lse_p) of query heads h0 .. h0+rows-1 of
-// sequence s into out: out = sum_p 2^(lse_p - LSE) o_p, LSE = log2 sum_p
-// 2^lse_p.  A partition marked +inf (bad metadata) zeroes the row.  Runs in
-// the CTA that arrived last, so it sits on the critical path of the row: all
-// loads of a phase are issued together (L2 latency once per phase, not once
-// per partition).  Partials written by other CTAs are read through L2
-// (ld.global.cg).  `w` is shared scratch of rows x (kFuseMergeMaxParts + 1)
-// floats.
-__device__ __noinline__ void merge_row_partials(const DecodeParams& p, int s, int h0, int rows, int nparts,
-                                                float* w) {
-    constexpr int MP = kFuseMergeMaxParts;
-    const int tid = threadIdx.x;
-    const int64_t row0 = (int64_t)s * p.num_q_heads + h0;
-    for (int i = tid; i < rows * nparts; i += blockDim.x) {
-        const int r = i / nparts, j = i - r * nparts;
-        w[r * MP + j] = __ldcg(p.part_lse + (row0 + r) * p.max_parts + j);
-    }
-    __syncthreads();
-    for (int r = tid; r < rows; r += blockDim.x) {
-        float M = -INFINITY;
-        for (int j = 0; j < nparts; ++j) M = fmaxf(M, w[r * MP + j]);
-        const bool bad = M == INFINITY;  // a bad row merges to exact zeros
-        float sum = 0.f;
-        for (int j = 0; j < nparts; ++j) {
-            const float e = bad ? 0.f : exp2f(w[r * MP + j] - M);
-            w[r * MP + j] = e;
-            sum += e;
-        }
-        w[rows * MP + r] = bad ? 0.f : 1.f / sum;
-    }
-    __syncthreads();
-    // one float4 of one row per item; every partition's load issued up front
-    for (int i = tid; i < rows * (kHeadDim / 4); i += blockDim.x) {
-        const int r = i / (kHeadDim / 4), c = i - r * (kHeadDim / 4);
-        const float4* po = reinterpret_cast<const float4*>(p.part_o + (row0 + r) * p.max_parts * kHeadDim) + c;
-        float4 v[MP];
-#pragma unroll
-        for (int j = 0; j < MP; ++j)
-            if (j < nparts) v[j] = __ldcg(po + j * (kHeadDim / 4));
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < MP; ++j)
-            if (j < nparts) {
-                const float wj = w[r * MP + j];
-                acc.x += wj * v[j].x;
-                acc.y += wj * v[j].y;
-                acc.z += wj * v[j].z;
-                acc.w += wj * v[j].w;
-            }
-        const float inv = w[rows * MP + r];
-        store_out(p, s, h0 + r, 4 * c, acc.x * inv);
-        store_out(p, s, h0 + r, 4 * c + 1, acc.y * inv);
-        store_out(p, s, h0 + r, 4 * c + 2, acc.z * inv);
-        store_out(p, s, h0 + r, 4 * c + 3, acc.w * inv);
-    }
-}
-
 // NH: 8-head n-tiles per CTA (1: up to 8 query heads of a group, 2: up to 16).
-template <bool kBF16, int BS, int NH, int NCW, int NST>
+// kPrefix: grouped decode -- attend only tokens prefix_lens[s] .. L-1 (the
+// shared prefix is the prefix kernel's), partial indices after the prefix's.
+template <bool kBF16, int BS, int NH, int NCW, int NST, bool kPrefix>
 __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB - 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeParams p) {
@@ -146,23 +91,54 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
     }
     pdl_wait();
 
-    const int L = p.context_lens[s];
-    const bool bad_len = L < 0 || L > p.len_limit;
-    if (bad_len || part * p.partition_size >= L) {
-        // Partition 0 owns the output of a sequence with nothing to attend
-        // (L == 0) or with an invalid length: zeros.
-        if (part == 0) {
-            if (bad_len && tid == 0) record_error(p.err, PKV_DEVERR_CONTEXT_LEN);
-            for (int i = tid; i < rows * D; i += blockDim.x) store_out(p, s, h0 + i / D, i % D, 0.f);
+    int L, tok0, nparts, pidx, narrive;
+    bool shared = false;  // grouped decode: s has a shared prefix; its group is checked before the epilogue
+    int fold = 0;         // grouped decode: prefix partials this CTA folds into its own result
+    if constexpr (kPrefix) {
+        const SeqSpan sp = seq_span(p, s, BS);
+        if (sp.err || part >= sp.nsuf) {
+            // Partition 0 owns the output of a sequence with nothing to
+            // attend (L == 0), with bad metadata, or whose shared prefix no
+            // group attended: zeros.  (L == prefix > 0 and attended: the
+            // prefix kernel wrote it.)
+            if (part == 0) {
+                int err = sp.err;
+                if (!err && sp.plen > 0 && !group_verified(p, s)) err = PKV_DEVERR_GROUP;
+                if (err || sp.L == 0) {
+                    if (err && tid == 0) record_error(p.err, err);
+                    for (int i = tid; i < rows * D; i += blockDim.x) store_out(p, s, h0 + i / D, i % D, 0.f);
+                }
+            }
+            return;
         }
-        return;
+        L = sp.L;
+        tok0 = sp.plen + part * p.partition_size;  // whole blocks: the prefix length is a multiple of BS
+        nparts = sp.npre + sp.nsuf;
+        pidx = sp.npre + part;
+        narrive = sp.nsuf;  // the prefix partials are complete: only this side's partitions arrive
+        shared = sp.plen > 0;
+        fold = folds_prefix(sp) ? sp.npre : 0;
+    } else {
+        L = p.context_lens[s];
+        const bool bad_len = L < 0 || L > p.len_limit;
+        if (bad_len || part * p.partition_size >= L) {
+            // Partition 0 owns the output of a sequence with nothing to attend
+            // (L == 0) or with an invalid length: zeros.
+            if (part == 0) {
+                if (bad_len && tid == 0) record_error(p.err, PKV_DEVERR_CONTEXT_LEN);
+                for (int i = tid; i < rows * D; i += blockDim.x) store_out(p, s, h0 + i / D, i % D, 0.f);
+            }
+            return;
+        }
+        tok0 = part * p.partition_size;
+        nparts = (L + p.partition_size - 1) / p.partition_size;
+        pidx = part;
+        narrive = nparts;
     }
-    const int tok0 = part * p.partition_size;
     const int tok1 = min(L, tok0 + p.partition_size);
     const int nblk = (tok1 - tok0 + BS - 1) / BS;
     const int blk0 = tok0 / BS;
-    const int nparts = (L + p.partition_size - 1) / p.partition_size;
-    const bool write_partial = p.split && nparts > 1;
+    const bool write_partial = p.split && nparts > 1 && !fold;
 
     uint8_t* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOffset);
@@ -175,6 +151,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
             mbar_init(empty0 + 8 * i, 1);
         }
         flags[0] = 0;
+        flags[2] = 0;
         fence_barrier_init();
     }
     __syncthreads();
@@ -249,6 +226,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
                 __syncwarp();
             }
         }
+        if constexpr (kPrefix) {
+            // off the streaming path: every load of the partition is issued
+            if (shared && lane == 0 && !group_verified(p, s)) flags[2] = 1;
+        }
     } else {
         // ------------------------------------------------------------ consumers
         QFrag<NH> qf;
@@ -285,6 +266,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
         }
     }
     __syncthreads();
+    if constexpr (kPrefix) {
+        if (flags[2]) {
+            // no group attended this sequence's shared prefix: partition 0
+            // zeroes the output, nothing else is written
+            if (part == 0) {
+                if (tid == 0) record_error(p.err, PKV_DEVERR_GROUP);
+                for (int i = tid; i < rows * D; i += blockDim.x) store_out(p, s, h0 + i / D, i % D, 0.f);
+            }
+            return;
+        }
+    }
 
     // ---- merge the per-warp states (stage memory is free now)
     float* red = reinterpret_cast<float*>(smem);      // [NCW][HT][kRedStride]
@@ -293,13 +285,65 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
     __syncthreads();
 
     const bool bad = fl != 0;
+    if constexpr (kPrefix) {
+        if (fold) {
+            // out = (2^lse_own o_own + sum_j 2^lse_j o_j) / (2^lse_own + sum_j 2^lse_j)
+            // over this partition and the prefix partials j < fold; every
+            // load of a row chunk is issued before any is used.
+            constexpr int MP = kFuseMergeMaxParts;
+            for (int i = tid; i < rows * (D / 4); i += blockDim.x) {
+                const int hr = i / (D / 4), c4 = i - hr * (D / 4);
+                const int64_t row = (int64_t)s * p.num_q_heads + h0 + hr;
+                const float* plse = p.part_lse + row * p.max_parts;
+                const float4* po = reinterpret_cast<const float4*>(p.part_o + row * p.max_parts * D) + c4;
+                float lj[MP];
+                float4 vj[MP];
+#pragma unroll
+                for (int j = 0; j < MP; ++j)
+                    if (j < fold) {
+                        lj[j] = __ldcg(plse + j);
+                        vj[j] = __ldcg(po + j * (D / 4));
+                    }
+                float lse;
+                float4 o;
+                o.x = combine_warps<NCW, HT>(red, ml, hr, 4 * c4, lse);
+                o.y = combine_warps<NCW, HT>(red, ml, hr, 4 * c4 + 1, lse);
+                o.z = combine_warps<NCW, HT>(red, ml, hr, 4 * c4 + 2, lse);
+                o.w = combine_warps<NCW, HT>(red, ml, hr, 4 * c4 + 3, lse);
+                float M = lse;
+#pragma unroll
+                for (int j = 0; j < MP; ++j)
+                    if (j < fold) M = fmaxf(M, lj[j]);
+                const bool zero = bad || M == INFINITY;  // +inf: a prefix partition saw bad metadata
+                const float w0 = zero ? 0.f : exp2f(lse - M);
+                float sum = w0;
+                float4 acc = make_float4(w0 * o.x, w0 * o.y, w0 * o.z, w0 * o.w);
+#pragma unroll
+                for (int j = 0; j < MP; ++j)
+                    if (j < fold) {
+                        const float wj = zero ? 0.f : exp2f(lj[j] - M);
+                        sum += wj;
+                        acc.x += wj * vj[j].x;
+                        acc.y += wj * vj[j].y;
+                        acc.z += wj * vj[j].z;
+                        acc.w += wj * vj[j].w;
+                    }
+                const float inv = zero ? 0.f : 1.f / sum;
+                store_out(p, s, h0 + hr, 4 * c4, acc.x * inv);
+                store_out(p, s, h0 + hr, 4 * c4 + 1, acc.y * inv);
+                store_out(p, s, h0 + hr, 4 * c4 + 2, acc.z * inv);
+                store_out(p, s, h0 + hr, 4 * c4 + 3, acc.w * inv);
+            }
+            return;
+        }
+    }
     for (int i = tid; i < rows * D; i += blockDim.x) {
         const int hr = i / D, d = i % D;
         float lse;
         const float o = combine_warps<NCW, HT>(red, ml, hr, d, lse);
         const int h = h0 + hr;
         if (write_partial) {
-            const int64_t idx = ((int64_t)s * p.num_q_heads + h) * p.max_parts + part;
+            const int64_t idx = ((int64_t)s * p.num_q_heads + h) * p.max_parts + pidx;
             p.part_o[idx * D + d] = bad ? 0.f : o;
             // +inf marks a partition whose metadata was bad: the merge zeroes the output.
             if (d == 0) p.part_lse[idx] = bad ? INFINITY : lse;
@@ -315,7 +359,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
         __threadfence();
         __syncthreads();
         if (tid == 0)
-            flags[1] = arrive_last(p.merge_ctr + (int64_t)s * gridDim.y + blockIdx.y, p.epoch, nparts) ? 1 : 0;
+            flags[1] = arrive_last(p.merge_ctr + (int64_t)s * gridDim.y + blockIdx.y, p.epoch, narrive) ? 1 : 0;
         __syncthreads();
         if (flags[1]) {
             __threadfence();
@@ -335,10 +379,11 @@ __global__ void __launch_bounds__(kHeadDim * kReduceGroups) reduce_kernel(const 
     pdl_wait();  // the decode kernel's partials must be complete
     const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
     const int d = tid % kHeadDim, grp = tid / kHeadDim;
-    const int L = p.context_lens[s];
-    if (L < 0 || L > p.len_limit) return;  // the decode kernel already zeroed it
-    const int np = (L + p.partition_size - 1) / p.partition_size;
-    if (np <= 1) return;                   // written directly by the decode kernel
+    const SeqSpan sp = seq_span(p, s, p.block_size);
+    if (sp.err) return;                   // the decode kernel already zeroed it
+    if (sp.plen > 0 && !group_verified(p, s)) return;
+    const int np = sp.npre + sp.nsuf;
+    if (np <= 1 || folds_prefix(sp)) return;  // written directly by the kernel that attended it
     const int64_t base = ((int64_t)s * p.num_q_heads + h) * p.max_parts;
     const float* lse = p.part_lse + base;
     const float* po = p.part_o + base * kHeadDim + d;
@@ -386,10 +431,12 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmk
     constexpr int NCW = PKV_NCW;
     constexpr int NST = BS == 16 ? PKV_NST16 : PKV_NST32;
     using S = DecodeSmem<BS, NCW, NST, 8 * NH>;
-    auto kern = decode_kernel<kBF16, BS, NH, NCW, NST>;
+    auto kern = p.prefix_lens ? decode_kernel<kBF16, BS, NH, NCW, NST, true>
+                              : decode_kernel<kBF16, BS, NH, NCW, NST, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kDynamic);
     if (e != cudaSuccess) return e;
-    const dim3 grid(p.max_parts, p.num_kv_heads * p.head_tiles, p.num_seqs);
+    // grouped decode: partitions of the sequences' own tokens only
+    const dim3 grid(p.max_parts - p.prefix_parts, p.num_kv_heads * p.head_tiles, p.num_seqs);
     e = launch_pdl(kern, grid, dim3((NCW + 1) * 32), S::kDynamic, stream, tmk, tmv, p);
     if (e != cudaSuccess) return e;
     ++*launches;
@@ -400,8 +447,6 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmk
     }
     return cudaSuccess;
 }
-
-int decode_head_tile(int group) { return group <= 8 ? 8 : 16; }
 
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int block_size, const CUtensorMap& tmk,
                           const CUtensorMap& tmv, cudaStream_t stream, int* launches) {

@@ -66,15 +66,39 @@ struct DecodeParams {
     int head_tiles;              // ceil(G / decode_head_tile(G))
     int out_dtype;               // pkv_dtype
     int split;                   // 1: sequences with > 1 partition write partials
+    int block_size;
     float scale_log2;            // scale * log2(e)
+    // grouped decode (paged_attention_decode_grouped): sequence s's first
+    // prefix_lens[s] tokens are attended by the prefix kernel through the
+    // block table of its group's first member, in prefix partitions of
+    // prefix_partition tokens (partial indices 0 .. npre-1); the decode
+    // kernel attends tokens prefix_lens[s] .. L-1 (partial indices npre ..).
+    const int32_t* prefix_lens;     // [B]; nullptr: plain decode
+    const int32_t* group_starts;    // [num_groups + 1]: members of group g are group_starts[g] .. [g+1]-1
+    int* seq_group;                 // [B]: group the prefix kernel took s into (a hint: see group_verified)
+    int max_prefix_len;
+    int prefix_partition;           // tokens, multiple of block_size
+    int prefix_parts;               // ceil(max_prefix_len / prefix_partition)
+    int num_groups;
+    int members_per_tile;           // group members per prefix CTA (whole members, <= 64 query rows)
+    int row_tiles;                  // prefix CTAs per (group, KV head, prefix partition)
 };
 
+// Prefix partition of grouped decode (tokens).
+constexpr int kPrefixPartition = 256;
+// Query rows of one prefix CTA (4 consumer warps x 16 rows).
+constexpr int kPrefixRows = 64;
+
 // Query heads of one GQA group handled by one decode CTA (8 or 16).
-int decode_head_tile(int group);
+__host__ __device__ inline int decode_head_tile(int group) { return group <= 8 ? 8 : 16; }
 
 // Host-side launchers (decode.cu); return a cudaError_t from the launch.
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int block_size, const CUtensorMap& tmk,
                           const CUtensorMap& tmv, cudaStream_t stream, int* launches);
+// Grouped decode: the shared-prefix kernel (group_prefix.cu), then the
+// decode kernel over each sequence's own tokens.
+cudaError_t launch_group_prefix(const DecodeParams& p, int dtype, int block_size, const CUtensorMap& tmk,
+                                const CUtensorMap& tmv, cudaStream_t stream, int* launches);
 
 struct AppendParams {
     int* err;

@@ -356,3 +356,92 @@ def fill_data(wl: Workload, threads: int | None = None) -> None:
     wl.q = normal(seed, S_Q, (wl.num_seqs, spec.num_q_heads, D), spec.dtype, threads=threads)
     wl.new_k = normal(seed, S_NEW_K, (T, hkv, D), spec.dtype, threads=threads)
     wl.new_v = normal(seed, S_NEW_V, (T, hkv, D), spec.dtype, threads=threads)
+
+
+def prefix_groups(wl: Workload) -> tuple[np.ndarray, np.ndarray, int]:
+    """Shared-prefix groups of a workload, as grouped decode takes them.
+
+    A group is a run of consecutive sequences with the same ``groups`` id (a
+    workload without one per sequence makes every sequence its own group).
+    A member's prefix length is the whole blocks its block table shares with
+    the group's first member, within both contexts; every member of a group
+    gets the smallest of these, and a group of one shares nothing.
+
+    Returns (group_starts int32 [num_groups + 1], prefix_lens int32 [B],
+    largest group size).
+    """
+    B, bs = wl.num_seqs, wl.block_size
+    ids = wl.groups if wl.groups is not None and len(wl.groups) == B else np.arange(B)
+    starts = [0] + [s for s in range(1, B) if ids[s] != ids[s - 1]] + [B]
+    plen = np.zeros(B, dtype=np.int32)
+    for a, b in zip(starts[:-1], starts[1:]):
+        if b - a < 2:
+            continue
+        common = None
+        for s in range(a + 1, b):
+            n = min(int(wl.context_lens[a]), int(wl.context_lens[s])) // bs
+            same = wl.block_tables[s, :n] == wl.block_tables[a, :n]
+            k = n if same.all() else int(np.argmin(same))
+            common = k if common is None else min(common, k)
+        plen[a:b] = common * bs
+    sizes = np.diff(starts)
+    return np.asarray(starts, dtype=np.int32), plen, int(sizes.max()) if len(sizes) else 1
+
+
+def make_grouped_workload(seed: int, members: list[list[tuple[int, int]]], num_q_heads: int, num_kv_heads: int,
+                          block_size: int, dtype: str, pool_factor: float = 1.25,
+                          threads: int | None = None) -> tuple[Workload, np.ndarray, np.ndarray, int]:
+    """A decode batch of forked groups for grouped decode, without a decode step's append.
+
+    ``members[g]`` lists (prefix_len, context_len) per member of group g, in
+    order; prefix lengths are multiples of ``block_size``.  The group's first
+    member is the parent: it holds the longest prefix, and each other member
+    is forked from it when the parent's context reaches that member's prefix
+    length, so the member shares exactly those blocks; every member then
+    writes its own tokens up to its context length.  A group of one with
+    prefix 0 is a plain sequence.
+
+    Returns (workload, group_starts, prefix_lens, largest group size).
+    """
+    bs = block_size
+    spec = Spec("grouped", 9, num_q_heads, num_kv_heads, bs, dtype, pool_factor=pool_factor)
+
+    def run(bm: BlockManager):
+        seq, lens, gid, plens, starts = 0, [], [], [], [0]
+        for g, mem in enumerate(members):
+            lead = seq
+            order = sorted(range(1, len(mem)), key=lambda i: mem[i][0])
+            top = max(p for p, _ in mem)
+            assert all(p % bs == 0 for p, _ in mem) and top <= mem[0][1] and all(p <= L for p, L in mem)
+            bm.add_sequence(lead)
+            for i in order:                          # parent grows; fork each member at its prefix
+                bm.append_tokens(lead, mem[i][0] - bm.num_tokens(lead))
+                bm.fork(lead, lead + i)
+            bm.append_tokens(lead, mem[0][1] - bm.num_tokens(lead))
+            for i in range(1, len(mem)):
+                bm.append_tokens(lead + i, mem[i][1] - bm.num_tokens(lead + i))
+            for i, (p, L) in enumerate(mem):
+                lens.append(L)
+                gid.append(g)
+                plens.append(p if i else (top if len(mem) > 1 else p))
+            seq += len(mem)
+            starts.append(seq)
+        return lens, gid, plens, starts
+
+    probe = BlockManager(1 << 22, bs)
+    run(probe)
+    num_blocks = max(1, math.ceil(pool_factor * ((1 << 22) - probe.num_free)))
+    bm = BlockManager(num_blocks, bs, permutation(seed, S_PERM, num_blocks))
+    lens, gid, plens, starts = run(bm)
+    B = len(lens)
+    tables = [bm.block_table(s) for s in range(B)]
+    maxb = max(1, max(len(t) for t in tables))
+    bt = np.full((B, maxb), -1, dtype=np.int32)
+    for s, t in enumerate(tables):
+        bt[s, : len(t)] = t
+    wl = Workload(spec=spec, seed=seed, num_blocks=num_blocks, context_lens=np.asarray(lens, dtype=np.int32),
+                  block_tables=bt, slot_mapping=np.zeros(0, dtype=np.int64), append_seq=np.zeros(0, dtype=np.int32),
+                  cow_pairs=np.zeros((0, 2), dtype=np.int64), groups=np.asarray(gid, dtype=np.int32))
+    fill_data(wl, threads=threads)
+    sizes = [len(m) for m in members]
+    return wl, np.asarray(starts, dtype=np.int32), np.asarray(plens, dtype=np.int32), max(sizes) if sizes else 1

@@ -28,7 +28,8 @@ def test_header_declares_the_entry_points():
     assert {"paged_kv_append", "paged_attention_decode", "copy_blocks", "paged_attention_workspace_bytes",
             "pkv_check_device_error", "pkv_status_string", "pkv_launch_count", "pkv_version",
             "paged_attention_partition_size", "paged_attention_plan", "paged_attention_append_decode",
-            "swap_blocks", "compact_tokens"} <= names
+            "swap_blocks", "compact_tokens", "paged_attention_decode_grouped",
+            "paged_attention_grouped_workspace_bytes", "paged_attention_decode_static"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -95,6 +96,39 @@ def test_workspace_bytes(lib):
     rows = 8 * 64 * 256
     assert n >= rows * 128 * 4 + rows * 4 and n % 256 == 0
     assert binding.paged_attention_workspace_bytes(-1, 64, 128, 10, 0) == 0
+
+
+def _grouped(lib, desc, hq=4, max_ctx=64, num_groups=1, max_group=4, max_prefix=32, gs=16, pl=16, ws=None,
+             ws_bytes=0, P=0):
+    ptr = 16
+    return lib.paged_attention_decode_grouped(ptr, ptr, ptr, ptr, 4, ptr, 2, hq, max_ctx, gs, num_groups, max_group,
+                                              pl, max_prefix, 0.1, ptr, binding.PKV_FP32, ctypes.byref(desc), P, ws,
+                                              ws_bytes, None)
+
+
+def test_grouped_host_validation(lib):
+    d = _desc()
+    assert _grouped(lib, d, hq=65) == binding.PKV_ERR_UNSUPPORTED               # > 64 query heads per KV head
+    assert _grouped(lib, d, max_prefix=80) == binding.PKV_ERR_INVALID_ARG       # above max_context_len
+    assert _grouped(lib, d, max_prefix=-16) == binding.PKV_ERR_INVALID_ARG
+    assert _grouped(lib, d, num_groups=-1) == binding.PKV_ERR_INVALID_ARG
+    assert _grouped(lib, d, max_group=0) == binding.PKV_ERR_INVALID_ARG
+    assert _grouped(lib, d, pl=None) == binding.PKV_ERR_INVALID_ARG              # prefix_lens missing
+    assert _grouped(lib, d, gs=None) == binding.PKV_ERR_INVALID_ARG              # group_starts missing
+    assert _grouped(lib, d, pl=18) == binding.PKV_ERR_INVALID_ARG                # misaligned
+    assert _grouped(lib, d) == binding.PKV_ERR_WORKSPACE                         # always needs one
+    assert _grouped(lib, d, ws=256, ws_bytes=1024) == binding.PKV_ERR_WORKSPACE  # too small
+
+
+def test_grouped_workspace_bytes(lib):
+    f = binding.paged_attention_grouped_workspace_bytes
+    # partials for ceil(1024 / 256) prefix + ceil(1551 / 512) own partitions per row, plus a group word per sequence
+    rows = 256 * 32 * (4 + 4)
+    n = f(256, 32, 128, 1551, 1024, 0)
+    assert n >= rows * 128 * 4 + rows * 4 + 256 * 4 and n % 256 == 0
+    assert f(256, 32, 128, 1551, 0, 0) > 0                   # needed even without a prefix
+    assert f(256, 32, 128, 100, 200, 0) == 0                 # prefix above the context bound
+    assert f(-1, 32, 128, 100, 0, 0) == 0
 
 
 def test_append_and_copy_host_validation(lib):

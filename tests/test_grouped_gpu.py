@@ -1,0 +1,281 @@
+"""Grouped decode (paged_attention_decode_grouped) against the fp64 oracle.
+
+Sequences forked from one prompt share its blocks; grouped decode reads the
+shared blocks once per (group, KV head) for all members and merges with each
+member's own tokens.  Its result must be plain decode's: the oracle (which
+knows nothing of groups) is the reference, pools must be untouched, and the
+plain GPU kernel must agree to within accumulation-order differences.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_11_gb300 as pkv
+from paged_kv_cache_11_gb300 import workload as W
+from tests.step_helpers import max_abs_err, oracle_step, to_bits, to_dev
+
+pytestmark = pytest.mark.gpu
+TOL = 5e-3
+PREFIX_LEN, GROUP = 6, 7  # PKV_DEVERR_PREFIX_LEN, PKV_DEVERR_GROUP
+
+
+def _dev(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def run_grouped(wl, gs, pl, mg, dev, kc=None, vc=None, partition_size=0, out_dtype=torch.float32, workspace=None,
+                max_prefix_len=None, out=None):
+    dt = wl.dtype
+    kc = to_dev(wl.k_cache, dt, dev) if kc is None else kc
+    vc = to_dev(wl.v_cache, dt, dev) if vc is None else vc
+    mpl = int(pl.max()) if max_prefix_len is None and len(pl) else (max_prefix_len or 0)
+    out = pkv.paged_attention_decode_grouped(
+        to_dev(wl.q, dt, dev), kc, vc, _dev(wl.block_tables, dev), _dev(wl.context_lens, dev), _dev(gs, dev),
+        _dev(pl, dev), wl.scale, max_group_size=mg, max_prefix_len=mpl, max_context_len=wl.max_context_len,
+        partition_size=partition_size, out_dtype=out_dtype, workspace=workspace, out=out)
+    torch.cuda.synchronize()
+    return kc, vc, out
+
+
+def oracle_out(wl):
+    out, status = oracle.decode(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale, wl.dtype,
+                                threads=8)
+    assert not status.any()
+    return out
+
+
+def _tol(out_dtype, ref):
+    half_ulp = {torch.float32: 0.0, torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11}[out_dtype]
+    return TOL + half_ulp * np.abs(ref)
+
+
+# ------------------------------------------------------------------ the shared-prefix decode step
+@pytest.mark.parametrize("bs", [16, 32])
+def test_shared_prefix_step(gpu, bs):
+    """Forked samples of 4 prompts: CoW copy + continuation append, then grouped decode."""
+    wl = W.make_workload("shared_prefix", groups=4, per_group=16, prefix=512, suffix=(32, 300), seed=21,
+                         block_size=bs)
+    wl.poison()
+    dev, dt = gpu, wl.dtype
+    kc, vc = to_dev(wl.k_cache, dt, dev), to_dev(wl.v_cache, dt, dev)
+    pkv.copy_blocks(kc, vc, _dev(wl.cow_pairs, dev))
+    pkv.paged_kv_append(to_dev(wl.new_k, dt, dev), to_dev(wl.new_v, dt, dev), _dev(wl.slot_mapping, dev), kc, vc)
+    gs, pl, mg = W.prefix_groups(wl)
+    assert (pl[:] == 512).all() and mg == 16
+    _, _, out = run_grouped(wl, gs, pl, mg, dev, kc=kc, vc=vc)
+    okc, ovc, ref = oracle_step(wl)
+    assert np.array_equal(to_bits(kc), okc) and np.array_equal(to_bits(vc), ovc)
+    assert max_abs_err(out, ref) <= TOL
+    plain = pkv.paged_attention_decode(to_dev(wl.q, dt, dev), kc, vc, _dev(wl.block_tables, dev),
+                                       _dev(wl.context_lens, dev), wl.scale, max_context_len=wl.max_context_len)
+    torch.cuda.synchronize()
+    assert float((plain - out).abs().max()) <= 2e-5
+    assert pkv.check_device_error() == 0
+
+
+# ------------------------------------------------------------------ randomised groups
+def _case(seed):
+    rng = np.random.default_rng(seed)
+    dtype = ["bf16", "fp16"][rng.integers(2)]
+    bs = [16, 32][rng.integers(2)]
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 3, 4, 5, 8, 12, 16, 20, 32, 64]))
+    if hkv * G > 256:
+        hkv = max(1, 256 // G)
+    members, total = [], 0
+    for _ in range(int(rng.integers(1, 6))):
+        n = int(rng.integers(1, 21))
+        if total + n > 40:
+            break
+        top = bs * int(rng.integers(0, 2200 // bs))
+        lead_L = top + (int(rng.integers(0, 700)) if rng.random() < 0.85 else 0)
+        mem = [(top, lead_L)]
+        for _ in range(n - 1):
+            r = rng.random()
+            p = top if r < 0.7 else bs * int(rng.integers(0, top // bs + 1))
+            L = p + (int(rng.integers(0, 700)) if rng.random() < 0.85 else 0)
+            mem.append((p, L))
+        members.append(mem)
+        total += n
+    if rng.random() < 0.3:
+        members.append([(0, 0)])                   # an empty sequence of its own
+    P = [0, 0, 0, 16, 64, 512][rng.integers(6)] // bs * bs
+    out_dtype = [torch.float32, torch.float32, torch.bfloat16, torch.float16][rng.integers(4)]
+    return dict(dtype=dtype, bs=bs, hkv=hkv, G=G, members=members, P=P, out_dtype=out_dtype)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_groups(gpu, seed):
+    c = _case(500 + seed)
+    wl, gs, pl, mg = W.make_grouped_workload(seed, c["members"], c["hkv"] * c["G"], c["hkv"], c["bs"], c["dtype"])
+    wl.poison()
+    kc, vc, out = run_grouped(wl, gs, pl, mg, gpu, partition_size=c["P"], out_dtype=c["out_dtype"])
+    assert np.array_equal(to_bits(kc), wl.k_cache) and np.array_equal(to_bits(vc), wl.v_cache)
+    ref = oracle_out(wl)
+    o = out.float().cpu().numpy()
+    assert np.isfinite(o).all(), c
+    err = np.abs(o - ref)
+    assert (err <= _tol(c["out_dtype"], ref)).all(), (c, float(err.max()))
+    assert pkv.check_device_error() == 0
+    if c["out_dtype"] == torch.float32:
+        plain = pkv.paged_attention_decode(to_dev(wl.q, wl.dtype, gpu), kc, vc, _dev(wl.block_tables, gpu),
+                                           _dev(wl.context_lens, gpu), wl.scale, max_context_len=wl.max_context_len)
+        torch.cuda.synchronize()
+        assert float((plain - out).abs().max()) <= 2e-5
+
+
+def test_many_prefix_partitions_use_the_merge_kernel(gpu):
+    """17 prefix partitions + the own tokens: more than the in-kernel merge takes."""
+    wl, gs, pl, mg = W.make_grouped_workload(7, [[(4352, 4400), (4352, 4500), (4096, 4097)], [(0, 900)]], 16, 4, 16,
+                                             "bf16")
+    wl.poison()
+    _, _, out = run_grouped(wl, gs, pl, mg, gpu)
+    assert max_abs_err(out, oracle_out(wl)) <= TOL
+    assert pkv.check_device_error() == 0
+
+
+@pytest.mark.parametrize("G,members", [
+    (64, [[(256, 300), (256, 256), (128, 600)]]),           # one member per row tile
+    (3, [[(512, 700)] + [(512, 520 + 7 * i) for i in range(24)]]),  # 21 members per tile, two tiles
+    (4, [[(256, 256), (256, 256)], [(512, 512)]]),         # no own tokens at all
+    (8, [[(0, 40), (0, 50)], [(16, 16)]]),                 # prefix 0 in a group; a group of one
+])
+def test_group_shapes(gpu, G, members):
+    wl, gs, pl, mg = W.make_grouped_workload(11, members, G * 2, 2, 16, "fp16")
+    wl.poison()
+    _, _, out = run_grouped(wl, gs, pl, mg, gpu)
+    assert max_abs_err(out, oracle_out(wl)) <= TOL
+    assert pkv.check_device_error() == 0
+
+
+# ------------------------------------------------------------------ bad metadata
+MEMBERS = [[(64, 100), (64, 80), (32, 90)], [(32, 70), (32, 40)], [(16, 50)]]
+
+
+def _bad_case(gpu, gs=None, pl_edit=None, mg=None, G=4, hkv=2):
+    wl, gs0, pl, mg0 = W.make_grouped_workload(3, MEMBERS, G * hkv, hkv, 16, "bf16")
+    wl.poison()
+    ref = oracle_out(wl)
+    pl = pl.copy()
+    if pl_edit:
+        for s, v in pl_edit.items():
+            pl[s] = v
+    _, _, out = run_grouped(wl, gs0 if gs is None else np.asarray(gs, dtype=np.int32), pl,
+                            mg0 if mg is None else mg, gpu, max_prefix_len=96)
+    return out.float().cpu().numpy(), ref, pkv.check_device_error()
+
+
+@pytest.mark.parametrize("edit", [{1: 40}, {2: 112}, {4: -16}, {0: 128}, {5: 96}])
+def test_bad_prefix_len_zeroes_that_sequence(gpu, edit):
+    """Not a multiple of the block size, beyond the context, negative: error 6, that output zero."""
+    out, ref, err = _bad_case(gpu, pl_edit=edit)
+    bad = next(iter(edit))
+    assert err == PREFIX_LEN
+    for t in range(out.shape[0]):
+        if t == bad:
+            assert (out[t] == 0).all()
+        else:  # including the members of a group whose first member is the bad one
+            assert np.abs(out[t] - ref[t]).max() <= TOL, t
+
+
+def test_sequence_outside_every_group_is_zeroed(gpu):
+    out, ref, err = _bad_case(gpu, gs=[0, 3, 5])   # sequence 5 (prefix 16) in no group
+    assert err == GROUP
+    assert (out[5] == 0).all()
+    assert np.abs(out[:5] - ref[:5]).max() <= TOL
+
+
+def test_members_beyond_the_row_tiles_are_zeroed(gpu):
+    """G = 64: one member per prefix CTA; max_group_size 2 leaves the third member of group 0 out."""
+    out, ref, err = _bad_case(gpu, mg=2, G=64, hkv=1)
+    assert err == GROUP
+    assert (out[2] == 0).all()
+    keep = [0, 1, 3, 4, 5]
+    assert np.abs(out[keep] - ref[keep]).max() <= TOL
+
+
+def test_out_of_order_group_starts_are_reported(gpu):
+    out, _, err = _bad_case(gpu, gs=[0, 3, 1, 6])
+    assert err == GROUP
+    assert np.isfinite(out).all()
+
+
+# ------------------------------------------------------------------ workspace and replay
+def test_workspace_contents_do_not_matter(gpu):
+    wl, gs, pl, mg = W.make_grouped_workload(4, MEMBERS * 3, 8, 2, 16, "bf16")
+    ref = oracle_out(wl)
+    need = pkv.paged_attention_grouped_workspace_bytes(wl.num_seqs, 8, 128, wl.max_context_len, int(pl.max()))
+    ws = torch.empty(need, dtype=torch.uint8, device=gpu)
+    for fill in (0xFF, 0x00, 0x7F, None):
+        if fill is None:
+            ws.copy_(torch.randint(0, 256, (need,), dtype=torch.uint8))
+        else:
+            ws.fill_(fill)
+        for _ in range(2):  # and reuse
+            _, _, out = run_grouped(wl, gs, pl, mg, gpu, workspace=ws)
+            assert max_abs_err(out, ref) <= TOL
+    assert pkv.check_device_error() == 0
+
+
+def test_grouped_decode_in_a_cuda_graph(gpu):
+    """Captured once, replayed with the group metadata changed in place between replays."""
+    dev = gpu
+    wl, gs, pl, mg = W.make_grouped_workload(9, MEMBERS * 2, 8, 2, 16, "bf16")
+    ref = oracle_out(wl)
+    dt = wl.dtype
+    q, kc, vc = to_dev(wl.q, dt, dev), to_dev(wl.k_cache, dt, dev), to_dev(wl.v_cache, dt, dev)
+    bt, cl = _dev(wl.block_tables, dev), _dev(wl.context_lens, dev)
+    gs_d, pl_d = _dev(gs, dev), _dev(pl, dev)
+    mpl = int(pl.max())
+    need = pkv.paged_attention_grouped_workspace_bytes(wl.num_seqs, 8, 128, wl.max_context_len, mpl)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    out = torch.empty((wl.num_seqs, 8, 128), dtype=torch.float32, device=dev)
+
+    def call():
+        pkv.paged_attention_decode_grouped(q, kc, vc, bt, cl, gs_d, pl_d, wl.scale, max_group_size=mg,
+                                           max_prefix_len=mpl, max_context_len=wl.max_context_len, out=out,
+                                           workspace=ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert max_abs_err(out, ref) <= TOL
+    assert pkv.check_device_error() == 0
+    # sequence 11 (a group of one with a 16-token prefix) leaves every group
+    gs_d.copy_(_dev(np.asarray(list(gs[:-2]) + [gs[-2]] * 2, dtype=np.int32), dev))
+    g.replay()
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert (o[11] == 0).all() and np.abs(o[:11] - ref[:11]).max() <= TOL
+    assert pkv.check_device_error() == GROUP
+    gs_d.copy_(_dev(gs, dev))
+    g.replay()
+    torch.cuda.synchronize()
+    assert max_abs_err(out, ref) <= TOL
+    assert pkv.check_device_error() == 0
+
+
+# ------------------------------------------------------------------ host-side checks
+def test_host_checks(gpu):
+    wl, gs, pl, mg = W.make_grouped_workload(2, MEMBERS, 8, 2, 16, "bf16")
+    with pytest.raises(pkv.PagedKVError) as e:   # max_prefix_len above max_context_len
+        run_grouped(wl, gs, pl, mg, gpu, max_prefix_len=wl.max_context_len + 16)
+    assert e.value.status == 1
+    with pytest.raises(pkv.PagedKVError) as e:   # workspace too small
+        run_grouped(wl, gs, pl, mg, gpu, workspace=torch.empty(256, dtype=torch.uint8, device=gpu))
+    assert e.value.status == 3
+    wl65, gs65, pl65, mg65 = W.make_grouped_workload(2, MEMBERS, 65, 1, 16, "bf16")
+    with pytest.raises(pkv.PagedKVError) as e:   # more than 64 query heads per KV head
+        run_grouped(wl65, gs65, pl65, mg65, gpu)
+    assert e.value.status == 2

@@ -240,3 +240,30 @@ def test_deferred_free_keeps_compaction_sources_out_of_later_targets():
     src1, dst1 = bm.compact(1, range(0, 48, 2), defer_free=True)
     assert not (set(d // 16 for d in dst0 + dst1) & old)
     assert bm.release_deferred() == 6 and bm.num_free == 12 - 4
+
+
+def test_grouped_workload_shares_exactly_the_requested_blocks():
+    members = [[(64, 100), (32, 40), (64, 64), (0, 17)], [(0, 33)], [(16, 16), (16, 50)]]
+    wl, gs, pl, mg = W.make_grouped_workload(5, members, 8, 2, 16, "bf16")
+    assert gs.tolist() == [0, 4, 5, 7] and mg == 4
+    assert pl.tolist() == [64, 32, 64, 0, 0, 16, 16]
+    assert wl.context_lens.tolist() == [100, 40, 64, 17, 33, 16, 50]
+    bt = wl.block_tables
+    for s, p in ((1, 32), (2, 64), (3, 0), (6, 16)):
+        lead = 0 if s < 4 else 5
+        n = p // 16
+        assert (bt[s, :n] == bt[lead, :n]).all()
+        own = bt[s, n:(wl.context_lens[s] + 15) // 16]
+        assert not set(own.tolist()) & set(bt[lead, :(wl.context_lens[lead] + 15) // 16].tolist())
+
+
+def test_prefix_groups_of_the_shared_prefix_workload():
+    """16 groups of 16 forked samples: 1024 prompt tokens in 64 shared blocks each."""
+    wl = W.make_workload("shared_prefix", with_data=False)
+    gs, pl, mg = W.prefix_groups(wl)
+    assert gs.tolist() == list(range(0, 257, 16)) and mg == 16
+    assert (pl == 1024).all()
+    # plain decode workloads: every sequence on its own, nothing shared
+    wl = W.make_workload("llama8b", num_seqs=5, with_data=False)
+    gs, pl, mg = W.prefix_groups(wl)
+    assert gs.tolist() == [0, 1, 2, 3, 4, 5] and (pl == 0).all() and mg == 1
