@@ -334,6 +334,7 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
     const Plan pl = make_plan(num_seqs, cache->num_kv_heads, head_tiles, max_context_len, partition_size);
     const int P = pl.partition, max_parts = pl.max_parts + prefix_parts;
     const bool split = grp || pl.kind != PKV_PLAN_SINGLE;
+    if (!grp && pl.max_parts > 65535) return PKV_ERR_UNSUPPORTED;  // one grid dimension per partition
     if (split && !have_ws) return PKV_ERR_WORKSPACE;
 
     int* err = error_word();

@@ -13,9 +13,14 @@
 // head tile of <= 16 query heads, sequence).  A partition is a run of
 // `partition_size` tokens (512 by default); when a sequence has more than one
 // partition, each CTA writes its normalised partial output and log-sum-exp
-// and reduce_kernel merges them (split-K).  All query heads of a GQA group
-// share one pass over each K/V tile, so a tile is read from HBM once per KV
-// head (once per 16 query heads when the group is larger than 16).
+// and the last partition to finish (or reduce_kernel, for many partitions)
+// merges them (split-K).  All query heads of a GQA group share one pass over
+// each K/V tile, so a tile is read from HBM once per KV head (once per 16
+// query heads when the group is larger than 16).  Partitions are numbered
+// from the end of each sequence and that number is the slowest grid
+// dimension: the hardware starts CTAs in linear index order, so every full
+// partition starts before any sequence's last, shorter one, and the short
+// ones fill the end of the launch (longest first).
 //
 // CTA layout: NCW consumer warps + 1 producer warp.
 //   producer: reads the partition's block ids (32 at a time, coalesced),
@@ -24,10 +29,12 @@
 //     stage j % NST, completing on that stage's "full" mbarrier.
 //   consumer warp w: takes blocks j = w, w + NCW, ...; per 16-token sub-block
 //     S = Q K^T with mma.sync m16n8k16 (Q rows = the head tile, padded to 16
-//     with zeros), masks tokens past the context, updates its own running
-//     max/sum, then O += P V with P split into a 16-bit high part and a
-//     16-bit residual so that P keeps ~16 significant bits.  It releases the
-//     stage on its "empty" mbarrier.
+//     with zeros; two interleaved score accumulators), masks tokens past the
+//     context, updates its own running max/sum (the max is raised only when a
+//     score exceeds it by more than 2^8, which skips the reduction and the
+//     rescale on most blocks), then O += P V with P split into a 16-bit high
+//     part and a 16-bit residual so that P keeps ~16 significant bits.  It
+//     releases the stage on its "empty" mbarrier.
 //   epilogue: the NCW per-warp (m, l, O) states are merged through shared
 //     memory in warp order (fixed, so the result depends only on logical
 //     token positions and never on physical block ids).
@@ -73,10 +80,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
     uint8_t* smem = smem_raw + (((raw_sa + 1023u) & ~1023u) - raw_sa);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int part = blockIdx.x;
-    const int kvh = blockIdx.y / p.head_tiles;
-    const int ht = blockIdx.y - kvh * p.head_tiles;
-    const int s = blockIdx.z;
+    // Grid: grouped decode (prefix, head group, sequence); plain decode (head
+    // group, sequence, partition counted from the end of the sequence), so
+    // that the hardware, which starts CTAs in linear index order, starts every
+    // full partition before any sequence's last, shorter one.
+    const int ygrp = kPrefix ? blockIdx.y : blockIdx.x;  // KV head x head tile
+    const int kvh = ygrp / p.head_tiles;
+    const int ht = ygrp - kvh * p.head_tiles;
+    const int s = kPrefix ? blockIdx.z : blockIdx.y;
     const int h0 = kvh * p.group + ht * HT;  // first query head of this CTA
     const int rows = min(HT, p.group - ht * HT);
 
@@ -91,10 +102,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
     }
     pdl_wait();
 
-    int L, tok0, nparts, pidx, narrive;
+    int L, tok0, nparts, pidx, narrive, part;
     bool shared = false;  // grouped decode: s has a shared prefix; its group is checked before the epilogue
     int fold = 0;         // grouped decode: prefix partials this CTA folds into its own result
     if constexpr (kPrefix) {
+        part = blockIdx.x;
         const SeqSpan sp = seq_span(p, s, BS);
         if (sp.err || part >= sp.nsuf) {
             // Partition 0 owns the output of a sequence with nothing to
@@ -121,17 +133,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
     } else {
         L = p.context_lens[s];
         const bool bad_len = L < 0 || L > p.len_limit;
-        if (bad_len || part * p.partition_size >= L) {
-            // Partition 0 owns the output of a sequence with nothing to attend
-            // (L == 0) or with an invalid length: zeros.
-            if (part == 0) {
-                if (bad_len && tid == 0) record_error(p.err, PKV_DEVERR_CONTEXT_LEN);
-                for (int i = tid; i < rows * D; i += blockDim.x) store_out(p, s, h0 + i / D, i % D, 0.f);
-            }
+        nparts = (bad_len || L == 0) ? 1 : (L + p.partition_size - 1) / p.partition_size;
+        const int from_end = blockIdx.z;
+        if (from_end >= nparts) return;  // the sequence has no such partition
+        part = nparts - 1 - from_end;
+        if (bad_len || L == 0) {
+            // The single partition of a sequence with nothing to attend
+            // (L == 0) or with an invalid length owns its output: zeros.
+            if (bad_len && tid == 0) record_error(p.err, PKV_DEVERR_CONTEXT_LEN);
+            for (int i = tid; i < rows * D; i += blockDim.x) store_out(p, s, h0 + i / D, i % D, 0.f);
             return;
         }
         tok0 = part * p.partition_size;
-        nparts = (L + p.partition_size - 1) / p.partition_size;
         pidx = part;
         narrive = nparts;
     }
@@ -248,7 +261,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
             }
             const int valid = min(BS, tok1 - (tok0 + jj * BS));  // >= 1
             const uint32_t kb = smem_addr(stages + st * S::kStageBytes);
-            attend_block<kBF16, BS, NH>(acc, qf, kb, kb + S::kTileBytes, valid, sl2, lane);
+            attend_block<kBF16, BS, NH, false, true>(acc, qf, kb, kb + S::kTileBytes, valid, sl2, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
         }
@@ -359,7 +372,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
         __threadfence();
         __syncthreads();
         if (tid == 0)
-            flags[1] = arrive_last(p.merge_ctr + (int64_t)s * gridDim.y + blockIdx.y, p.epoch, narrive) ? 1 : 0;
+            flags[1] = arrive_last(p.merge_ctr + (int64_t)s * p.num_kv_heads * p.head_tiles + ygrp, p.epoch, narrive)
+                           ? 1
+                           : 0;
         __syncthreads();
         if (flags[1]) {
             __threadfence();
@@ -436,7 +451,8 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmk
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kDynamic);
     if (e != cudaSuccess) return e;
     // grouped decode: partitions of the sequences' own tokens only
-    const dim3 grid(p.max_parts - p.prefix_parts, p.num_kv_heads * p.head_tiles, p.num_seqs);
+    const dim3 grid = p.prefix_lens ? dim3(p.max_parts - p.prefix_parts, p.num_kv_heads * p.head_tiles, p.num_seqs)
+                                    : dim3(p.num_kv_heads * p.head_tiles, p.num_seqs, p.max_parts);
     e = launch_pdl(kern, grid, dim3((NCW + 1) * 32), S::kDynamic, stream, tmk, tmv, p);
     if (e != cudaSuccess) return e;
     ++*launches;
