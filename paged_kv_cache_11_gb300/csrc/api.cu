@@ -334,7 +334,6 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
     const Plan pl = make_plan(num_seqs, cache->num_kv_heads, head_tiles, max_context_len, partition_size);
     const int P = pl.partition, max_parts = pl.max_parts + prefix_parts;
     const bool split = grp || pl.kind != PKV_PLAN_SINGLE;
-    if (!grp && pl.max_parts > 65535) return PKV_ERR_UNSUPPORTED;  // one grid dimension per partition
     if (split && !have_ws) return PKV_ERR_WORKSPACE;
 
     int* err = error_word();
@@ -386,6 +385,7 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
     p.out_dtype = out_dtype;
     p.split = split ? 1 : 0;
     p.block_size = cache->block_size;
+    p.parts_in_x = max_parts > 65535 ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     if (fused_append) {
         p.fused_append = 1;

@@ -84,10 +84,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
     // group, sequence, partition counted from the end of the sequence), so
     // that the hardware, which starts CTAs in linear index order, starts every
     // full partition before any sequence's last, shorter one.
-    const int ygrp = kPrefix ? blockIdx.y : blockIdx.x;  // KV head x head tile
+    // (More than 65535 partitions do not fit the slowest dimension; such a
+    // call uses the grouped layout with the partition in x.)
+    const bool part_x = kPrefix || p.parts_in_x;
+    const int ygrp = part_x ? blockIdx.y : blockIdx.x;  // KV head x head tile
     const int kvh = ygrp / p.head_tiles;
     const int ht = ygrp - kvh * p.head_tiles;
-    const int s = kPrefix ? blockIdx.z : blockIdx.y;
+    const int s = part_x ? blockIdx.z : blockIdx.y;
     const int h0 = kvh * p.group + ht * HT;  // first query head of this CTA
     const int rows = min(HT, p.group - ht * HT);
 
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
         L = p.context_lens[s];
         const bool bad_len = L < 0 || L > p.len_limit;
         nparts = (bad_len || L == 0) ? 1 : (L + p.partition_size - 1) / p.partition_size;
-        const int from_end = blockIdx.z;
+        const int from_end = part_x ? blockIdx.x : blockIdx.z;
         if (from_end >= nparts) return;  // the sequence has no such partition
         part = nparts - 1 - from_end;
         if (bad_len || L == 0) {
@@ -451,8 +454,9 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmk
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kDynamic);
     if (e != cudaSuccess) return e;
     // grouped decode: partitions of the sequences' own tokens only
-    const dim3 grid = p.prefix_lens ? dim3(p.max_parts - p.prefix_parts, p.num_kv_heads * p.head_tiles, p.num_seqs)
-                                    : dim3(p.num_kv_heads * p.head_tiles, p.num_seqs, p.max_parts);
+    const dim3 grid = p.prefix_lens || p.parts_in_x
+                          ? dim3(p.max_parts - p.prefix_parts, p.num_kv_heads * p.head_tiles, p.num_seqs)
+                          : dim3(p.num_kv_heads * p.head_tiles, p.num_seqs, p.max_parts);
     e = launch_pdl(kern, grid, dim3((NCW + 1) * 32), S::kDynamic, stream, tmk, tmv, p);
     if (e != cudaSuccess) return e;
     ++*launches;

@@ -82,6 +82,7 @@ struct DecodeParams {
     int num_groups;
     int members_per_tile;           // group members per prefix CTA (whole members, <= 64 query rows)
     int row_tiles;                  // prefix CTAs per (group, KV head, prefix partition)
+    int parts_in_x;                 // plain decode with > 65535 partitions: partition index in grid x
 };
 
 // Prefix partition of grouped decode (tokens).

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import oracle
+import paged_kv_cache_11_gb300 as pkv
 from paged_kv_cache_11_gb300 import workload as W
 from tests.step_helpers import gpu_step, max_abs_err, oracle_step, single_token_step, to_bits, to_dev
 
@@ -129,6 +130,25 @@ def test_physical_permutation_is_bitwise_invisible(gpu):
     _, _, oa = gpu_step(a, gpu, partition_size=32)
     _, _, ob = gpu_step(b, gpu, partition_size=32)
     assert torch.equal(oa, ob)
+
+
+def test_more_partitions_than_one_grid_dimension(gpu):
+    """65600 one-block partitions, more than one grid dimension holds.  The
+    sequence's block table repeats the same 64 blocks 1025 times, and a
+    softmax over tokens that each appear n times is the softmax over one copy,
+    so the 1,049,600-token result is the oracle's over the first 1024 tokens."""
+    wl = W.make_workload("tiny", num_seqs=1, lens=("fixed", (1024,)), pool_blocks=64, seed=21)
+    reps = 1025
+    L = 1024 * reps
+    bt = np.tile(wl.block_tables[:, :64], (1, reps)).astype(np.int32)
+    ref, status = oracle.decode(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale, wl.dtype)
+    assert not status.any()
+    kc, vc, q = to_dev(wl.k_cache, wl.dtype, gpu), to_dev(wl.v_cache, wl.dtype, gpu), to_dev(wl.q, wl.dtype, gpu)
+    out = pkv.paged_attention_decode(q, kc, vc, torch.from_numpy(bt).to(gpu),
+                                     torch.tensor([L], dtype=torch.int32, device=gpu), wl.scale,
+                                     max_context_len=L, partition_size=16)
+    assert pkv.check_device_error() == 0
+    assert max_abs_err(out, ref) <= TOL
 
 
 def test_split_k_matches_single_pass(gpu):
