@@ -89,8 +89,8 @@ static WorkspaceLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, i
 }
 
 // Prefix partitions of grouped decode for the longest shared prefix.
-static int64_t prefix_parts_of(int64_t max_prefix_len) {
-    return (max_prefix_len + kPrefixPartition - 1) / kPrefixPartition;
+static int64_t prefix_parts_of(int64_t max_prefix_len, int64_t partition = kPrefixPartition) {
+    return (max_prefix_len + partition - 1) / partition;
 }
 
 // Epoch of a decode call: a process-wide counter, 48 bits, never 0.
@@ -143,6 +143,19 @@ static int resolve_partition(int32_t partition_size, int64_t rows, int32_t max_c
     return best;
 }
 
+
+// Tokens per prefix partition of grouped decode: the largest of 256, 512,
+// 1024 for which the prefix CTAs (group x KV head x row tile x partition,
+// counted at max_prefix_len) still fill three quarters of the device's
+// resident prefix CTAs (two per SM).  Fewer, longer partitions leave fewer
+// partials to merge; below that count the launch leaves SMs idle.
+static int resolve_prefix_partition(int64_t tiles, int32_t max_prefix_len) {
+    const int64_t slots = (int64_t)(sm_count() > 0 ? sm_count() : 148) * 2;
+    int best = kPrefixPartition;
+    for (int P = 2 * kPrefixPartition; P <= kPrefixPartitionMax; P *= 2)
+        if (4 * tiles * prefix_parts_of(max_prefix_len, P) >= 3 * slots) best = P;
+    return best;
+}
 
 // How a decode call divides its work (see paged_attention_plan).
 struct Plan {
@@ -311,7 +324,7 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
                          !aligned(slot_mapping, 8)))
         return PKV_ERR_INVALID_ARG;
 
-    int members_per_tile = 0, row_tiles = 0, prefix_parts = 0;
+    int members_per_tile = 0, row_tiles = 0, prefix_parts = 0, prefix_partition = kPrefixPartition;
     if (grp) {
         if (group > kPrefixRows) return PKV_ERR_UNSUPPORTED;
         if (grp->num_groups < 0 || grp->num_groups > 65535 || grp->max_prefix_len < 0 ||
@@ -323,7 +336,9 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
         members_per_tile = kPrefixRows / group;
         row_tiles = grp->num_groups > 0 ? (grp->max_group_size + members_per_tile - 1) / members_per_tile : 0;
         if ((int64_t)cache->num_kv_heads * row_tiles > 65535) return PKV_ERR_UNSUPPORTED;
-        prefix_parts = (int)prefix_parts_of(grp->max_prefix_len);
+        prefix_partition = resolve_prefix_partition(
+            (int64_t)grp->num_groups * cache->num_kv_heads * row_tiles, grp->max_prefix_len);
+        prefix_parts = (int)prefix_parts_of(grp->max_prefix_len, prefix_partition);
     }
     const size_t need = grp ? paged_attention_grouped_workspace_bytes(num_seqs, num_q_heads, kHeadDim,
                                                                       max_context_len, grp->max_prefix_len,
@@ -364,7 +379,7 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
             p.prefix_lens = grp->prefix_lens;
             p.group_starts = grp->group_starts;
             p.max_prefix_len = grp->max_prefix_len;
-            p.prefix_partition = kPrefixPartition;
+            p.prefix_partition = prefix_partition;
             p.prefix_parts = prefix_parts;
             p.num_groups = grp->num_groups;
             p.members_per_tile = members_per_tile;

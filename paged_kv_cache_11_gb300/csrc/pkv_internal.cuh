@@ -85,8 +85,10 @@ struct DecodeParams {
     int parts_in_x;                 // plain decode with > 65535 partitions: partition index in grid x
 };
 
-// Prefix partition of grouped decode (tokens).
+// Prefix partitions of grouped decode (tokens): chosen per call between the
+// smallest (which sizes the workspace) and the largest.
 constexpr int kPrefixPartition = 256;
+constexpr int kPrefixPartitionMax = 1024;
 // Query rows of one prefix CTA (4 consumer warps x 16 rows).
 constexpr int kPrefixRows = 64;
 

@@ -74,6 +74,30 @@ def test_shared_prefix_step(gpu, bs):
     assert pkv.check_device_error() == 0
 
 
+@pytest.mark.parametrize("groups", [16, 32])
+def test_long_prefix_partitions(gpu, groups):
+    """Enough groups for the call to take longer prefix partitions (on one
+    GB300: 512 tokens for 16 groups of a 1024-token prompt over 8 KV heads,
+    1024 tokens for 32 groups)."""
+    wl = W.make_workload("shared_prefix", groups=groups, per_group=2, prefix=1024, suffix=(32, 200), seed=40 + groups)
+    wl.poison()
+    dev, dt = gpu, wl.dtype
+    kc, vc = to_dev(wl.k_cache, dt, dev), to_dev(wl.v_cache, dt, dev)
+    pkv.copy_blocks(kc, vc, _dev(wl.cow_pairs, dev))
+    pkv.paged_kv_append(to_dev(wl.new_k, dt, dev), to_dev(wl.new_v, dt, dev), _dev(wl.slot_mapping, dev), kc, vc)
+    gs, pl, mg = W.prefix_groups(wl)
+    assert (pl[:] == 1024).all()
+    _, _, out = run_grouped(wl, gs, pl, mg, dev, kc=kc, vc=vc)
+    okc, ovc, ref = oracle_step(wl)
+    assert np.array_equal(to_bits(kc), okc) and np.array_equal(to_bits(vc), ovc)
+    assert max_abs_err(out, ref) <= TOL
+    plain = pkv.paged_attention_decode(to_dev(wl.q, dt, dev), kc, vc, _dev(wl.block_tables, dev),
+                                       _dev(wl.context_lens, dev), wl.scale, max_context_len=wl.max_context_len)
+    torch.cuda.synchronize()
+    assert float((plain - out).abs().max()) <= 2e-5
+    assert pkv.check_device_error() == 0
+
+
 # ------------------------------------------------------------------ randomised groups
 def _case(seed):
     rng = np.random.default_rng(seed)
