@@ -540,6 +540,12 @@ def run_ours(args):
         cpu = {"value": b / t / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{reps} oracle step(s) over the first {n} of {wl.num_seqs} sequences (all query "
                          f"heads), {t:.1f} s on {threads} host threads"}
+        # the same oracle on one thread, over fewer sequences (about 3 s)
+        n1 = max(1, int(n * min(1.0, 3.0 / max(threads * t / reps, 1e-9))))
+        dt1, b1, n1 = time_oracle(wl, n1, 1)
+        cpu["single_thread"] = {"value": b1 / dt1 / 1e9, "unit": UNIT, "cores": 1,
+                                "sample": f"one oracle step over the first {n1} of {wl.num_seqs} sequences, "
+                                          f"{dt1:.1f} s on 1 host thread"}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps, "warmup": args.warmup,
