@@ -55,6 +55,9 @@ def parse_args(argv=None):
     ap.add_argument("--unfused", action="store_true", help="separate block-write and decode launches")
     ap.add_argument("--ungrouped", action="store_true",
                     help="shared-prefix workloads: plain paged_attention_decode instead of the grouped call")
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="write a 256 MB buffer before every step (outside the step's timing) so that no step "
+                         "finds the previous one's K/V in L2")
     return ap.parse_args(argv)
 
 
@@ -386,7 +389,12 @@ def run_ours(args):
     # loop, and that launch's duration is the step's.  A step of several
     # launches also brackets its decode call with events.
     evs = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-           if not fused else [None] * args.steps)
+           if not fused or args.flush_l2 else [None] * args.steps)
+    # --flush-l2: each step is bracketed by its own events and the flush runs
+    # between steps, outside them
+    step_evs = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)] if args.flush_l2 else None)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
@@ -396,7 +404,12 @@ def run_ours(args):
     l0 = pkv.launch_count()
     t_start.record(stream)
     for i in range(args.steps):
+        if flush_buf is not None:
+            flush_buf.zero_()
+            step_evs[i][0].record(stream)
         step(evs[i])
+        if flush_buf is not None:
+            step_evs[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     launches = pkv.launch_count() - l0
@@ -405,7 +418,9 @@ def run_ours(args):
     if dist:
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
-    if fused:
+    if step_evs is not None:
+        ms_total = sum(a.elapsed_time(b) for a, b in step_evs)  # the steps alone, without the flushes
+    if fused and step_evs is None:
         dec_avg_ms = ms_total / args.steps
     else:
         dec_ms = [a.elapsed_time(b) for a, b in evs]
@@ -552,7 +567,8 @@ def run_ours(args):
         "ms_per_step": ms_max / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic",
         "config": {**describe(wl), "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": f"inputs larger than L2 ({wl.kv_bytes() / 1e6:.0f} MB of K/V vs 129 MB), no flush",
+                   "l2": ("256 MB written before every step, outside the step's timing" if args.flush_l2 else
+                          f"inputs larger than L2 ({wl.kv_bytes() / 1e6:.0f} MB of K/V vs 129 MB), no flush"),
                    "api": dec_api if fused else "copy_blocks + paged_kv_append + " + dec_api,
                    "partition_size": pkv.paged_attention_partition_size(
                        wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, mcl, args.partition_size)},

@@ -62,36 +62,6 @@ struct DecodeSmem {
     static constexpr int kDynamic = kTotal + 1024;        // slack to align the base to 1024 B
 };
 
-// Single-pass batches of at most this many sequences start their CTAs
-// longest sequence first (seq_of_rank).
-constexpr int kRankedSeqs = 256;
-
-// The sequence whose last partition (the one holding its final tokens; in a
-// single-pass call, the whole context) is the rank-th largest, ties by
-// sequence index; rows with nothing to attend (L == 0 or a bad length) rank
-// last.  Every thread of the CTA takes part;
-// `scratch` is shared memory for kRankedSeqs + 1 ints, free until the
-// pipeline starts.
-static __device__ __noinline__ int seq_of_rank(const DecodeParams& p, int rank, int* scratch) {
-    const int B = p.num_seqs, P = p.partition_size;
-    for (int t = threadIdx.x; t < B; t += blockDim.x) {
-        const int L = p.context_lens[t];
-        scratch[t] = (L <= 0 || L > p.len_limit) ? 0 : L - ((L - 1) / P) * P;
-    }
-    __syncthreads();
-    for (int t = threadIdx.x; t < B; t += blockDim.x) {
-        const int lt = scratch[t];
-        int r = 0;
-        for (int u = 0; u < B; ++u) {
-            const int lu = scratch[u];
-            r += lu > lt || (lu == lt && u < t);
-        }
-        if (r == rank) scratch[kRankedSeqs] = t;
-    }
-    __syncthreads();
-    return scratch[kRankedSeqs];
-}
-
 // NH: 8-head n-tiles per CTA (1: up to 8 query heads of a group, 2: up to 16).
 // kPrefix: grouped decode -- attend only tokens prefix_lens[s] .. L-1 (the
 // shared prefix is the prefix kernel's), partial indices after the prefix's.
@@ -120,7 +90,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
     const int ygrp = part_x ? blockIdx.y : blockIdx.x;  // KV head x head tile
     const int kvh = ygrp / p.head_tiles;
     const int ht = ygrp - kvh * p.head_tiles;
-    int s = part_x ? blockIdx.z : blockIdx.y;
+    const int s = part_x ? blockIdx.z : blockIdx.y;
     const int h0 = kvh * p.group + ht * HT;  // first query head of this CTA
     const int rows = min(HT, p.group - ht * HT);
 
@@ -165,12 +135,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
         fold = folds_prefix(sp) ? sp.npre : 0;
     } else {
         const int from_end = part_x ? blockIdx.x : blockIdx.z;
-        // A single-pass call starts its CTAs longest sequence first: grid
-        // index y is a rank, not a sequence.  (Ranking the last, shorter
-        // partitions of a split call measured slower than leaving them in
-        // sequence order.)
-        if (p.max_parts == 1 && !part_x && p.num_seqs <= kRankedSeqs)
-            s = seq_of_rank(p, s, reinterpret_cast<int*>(smem));
         L = p.context_lens[s];
         const bool bad_len = L < 0 || L > p.len_limit;
         nparts = (bad_len || L == 0) ? 1 : (L + p.partition_size - 1) / p.partition_size;

@@ -37,6 +37,23 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_header_compiles_and_links_as_c(lib, tmp_path):
+    """The boundary is a C ABI: a C99 program includes the header, links every
+    entry point from the library and runs the calls that need no GPU."""
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        pytest.skip("gcc not found")
+    exe = tmp_path / "abi_c_program"
+    src = Path(__file__).resolve().parent / "abi_c_program.c"
+    libdir = binding.LIB_PATH.parent
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", str(HEADER.parent), str(src), "-o",
+                        str(exe), "-L", str(libdir), "-lpagedkv", f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "c abi ok" in r.stdout, (r.returncode, r.stdout, r.stderr)
+
+
 def test_built_for_sm_103a_only():
     src = (Path(_build.__file__)).read_text()
     assert "arch=compute_103a,code=sm_103a" in src
