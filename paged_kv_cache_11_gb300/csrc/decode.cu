@@ -18,9 +18,12 @@
 // each K/V tile, so a tile is read from HBM once per KV head (once per 16
 // query heads when the group is larger than 16).  Partitions are numbered
 // from the end of each sequence and that number is the slowest grid
-// dimension: the hardware starts CTAs in linear index order, so every full
-// partition starts before any sequence's last, shorter one, and the short
-// ones fill the end of the launch (longest first).
+// dimension.  The hardware starts CTAs in linear index order, so every
+// sequence's last partition (usually shorter than the others) starts first,
+// then the full partitions before it, and the first partitions of the
+// sequences with the most partitions end the launch.  This order measured
+// faster than starting from the first partitions, and faster than running
+// all full partitions before the last ones.
 //
 // CTA layout: NCW consumer warps + 1 producer warp.
 //   producer: reads the partition's block ids (32 at a time, coalesced),
@@ -81,9 +84,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Grid: grouped decode (prefix, head group, sequence); plain decode (head
-    // group, sequence, partition counted from the end of the sequence), so
-    // that the hardware, which starts CTAs in linear index order, starts every
-    // full partition before any sequence's last, shorter one.
+    // group, sequence, partition counted from the end of the sequence): the
+    // hardware starts CTAs in linear index order, so the last partitions of
+    // all sequences start first.
     // (More than 65535 partitions do not fit the slowest dimension; such a
     // call uses the grouped layout with the partition in x.)
     const bool part_x = kPrefix || p.parts_in_x;
