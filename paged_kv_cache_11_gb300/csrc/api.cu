@@ -52,17 +52,34 @@ static EncodeTiledFn encode_fn() {
 
 // The pool viewed as a 2-D tensor [num_blocks * Hkv * bs rows][128 columns];
 // box = one 64-column half of a (block, KV head) tile, 128-byte swizzle.
-static pkv_status encode_cache_map(CUtensorMap* m, const void* base, const pkv_cache_desc& c) {
+// Tensor maps of a K or V pool, 128-byte swizzle (a 64-element, 128-byte
+// row per line).  Rank 2: the pool as [rows][128] (rows = blocks x KV heads
+// x block size), box [BS][64]: one copy brings one dims half of a (block,
+// KV head) tile.  Rank 3: the same memory as [2 halves][rows][64], the two
+// halves of a row 128 bytes apart, box [2][BS][64]: one copy brings the
+// whole tile as its two halves back to back, the layout the rank-2 copies
+// of both halves give.  Every coordinate stays inside the pool.
+static pkv_status encode_cache_map(CUtensorMap* m, const void* base, const pkv_cache_desc& c, int rank) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return PKV_ERR_CUDA;
-    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)c.num_blocks * c.num_kv_heads * c.block_size};
-    const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)c.block_size};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r =
-        fn(m, c.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const cuuint64_t rows = (cuuint64_t)c.num_blocks * c.num_kv_heads * c.block_size;
+    const CUtensorMapDataType dt =
+        c.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r;
+    if (rank == 2) {
+        const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)c.block_size};
+        r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[3] = {64, rows, 2};
+        const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, 128};
+        const cuuint32_t box[3] = {64, (cuuint32_t)c.block_size, 2};
+        r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_INVALID_ARG;
 }
 
@@ -147,10 +164,10 @@ static int resolve_partition(int32_t partition_size, int64_t rows, int32_t max_c
 // Tokens per prefix partition of grouped decode: the largest of 256, 512,
 // 1024 for which the prefix CTAs (group x KV head x row tile x partition,
 // counted at max_prefix_len) still fill three quarters of the device's
-// resident prefix CTAs (two per SM).  Fewer, longer partitions leave fewer
-// partials to merge; below that count the launch leaves SMs idle.
+// resident prefix CTAs (kPrefixCtasPerSm per SM).  Fewer, longer partitions
+// leave fewer partials to merge; below that count the launch leaves SMs idle.
 static int resolve_prefix_partition(int64_t tiles, int32_t max_prefix_len) {
-    const int64_t slots = (int64_t)(sm_count() > 0 ? sm_count() : 148) * 2;
+    const int64_t slots = (int64_t)(sm_count() > 0 ? sm_count() : 148) * kPrefixCtasPerSm;
     int best = kPrefixPartition;
     for (int P = 2 * kPrefixPartition; P <= kPrefixPartitionMax; P *= 2)
         if (4 * tiles * prefix_parts_of(max_prefix_len, P) >= 3 * slots) best = P;
@@ -353,11 +370,17 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
 
     int* err = error_word();
     if (!err) return PKV_ERR_CUDA;
-    CUtensorMap tmk, tmv;
-    st = encode_cache_map(&tmk, k_cache, *cache);
+    // whole tiles (rank 3) for the decode kernel and for V in the prefix
+    // kernel; the prefix kernel's K chunks need one copy per dims half (rank 2)
+    CUtensorMap tmk, tmv, tmk_half;
+    st = encode_cache_map(&tmk, k_cache, *cache, 3);
     if (st != PKV_OK) return st;
-    st = encode_cache_map(&tmv, v_cache, *cache);
+    st = encode_cache_map(&tmv, v_cache, *cache, 3);
     if (st != PKV_OK) return st;
+    if (grp) {
+        st = encode_cache_map(&tmk_half, k_cache, *cache, 2);
+        if (st != PKV_OK) return st;
+    }
 
     DecodeParams p;
     std::memset(&p, 0, sizeof(p));
@@ -413,7 +436,7 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
     int launches = 0;
     cudaError_t e = cudaSuccess;
     if (grp && prefix_parts > 0 && grp->num_groups > 0)
-        e = launch_group_prefix(p, cache->dtype, cache->block_size, tmk, tmv, static_cast<cudaStream_t>(stream),
+        e = launch_group_prefix(p, cache->dtype, cache->block_size, tmk_half, tmv, static_cast<cudaStream_t>(stream),
                                 &launches);
     if (e == cudaSuccess)
         e = launch_decode(p, cache->dtype, cache->block_size, tmk, tmv, static_cast<cudaStream_t>(stream), &launches);

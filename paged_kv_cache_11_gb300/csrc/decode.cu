@@ -27,9 +27,11 @@
 //
 // CTA layout: NCW consumer warps + 1 producer warp.
 //   producer: reads the partition's block ids (32 at a time, coalesced),
-//     checks them against the pool, and for block j issues four 2-D TMA
-//     loads (K and V, two 64-column halves each, 128-byte swizzle) into ring
-//     stage j % NST, completing on that stage's "full" mbarrier.
+//     checks them against the pool, and for block j issues two TMA loads
+//     (K and V; each brings the tile's two 64-column halves, 128-byte
+//     swizzle) into ring stage j % NST, completing on that stage's "full"
+//     mbarrier.  One copy per tile rather than per half: the SM's TMA unit
+//     takes a roughly fixed time per copy of this size.
 //   consumer warp w: takes blocks j = w, w + NCW, ...; per 16-token sub-block
 //     S = Q K^T with mma.sync m16n8k16 (Q rows = the head tile, padded to 16
 //     with zeros; two interleaved score accumulators), masks tokens past the
@@ -232,10 +234,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
                         mbar_arrive_expect_tx(fb, S::kStageBytes);
                         const uint32_t dst = smem_addr(stages + st * S::kStageBytes);
                         const int y = (pid * p.num_kv_heads + kvh) * BS;  // row of the tile in [rows][128]
-                        tma_load_2d(dst, &tmk, fb, 0, y, policy);
-                        tma_load_2d(dst + S::kHalfBytes, &tmk, fb, 64, y, policy);
-                        tma_load_2d(dst + S::kTileBytes, &tmv, fb, 0, y, policy);
-                        tma_load_2d(dst + S::kTileBytes + S::kHalfBytes, &tmv, fb, 64, y, policy);
+                        tma_load_3d(dst, &tmk, fb, 0, y, 0, policy);  // both dims halves of the tile
+                        tma_load_3d(dst + S::kTileBytes, &tmv, fb, 0, y, 0, policy);
                         ++issued;
                     } else {
                         atomicOr(flags, 2);

@@ -1,4 +1,5 @@
-// group_prefix.cu -- the shared-prefix half of grouped decode.
+// group_prefix.cu -- the shared-prefix half of grouped decode, on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 // Sequences forked from one prompt (parallel samples, beams, a common
 // system prompt) hold the prompt's K/V in the same physical blocks: the
@@ -15,54 +16,184 @@
 // softmax over a union of token sets is the weighted merge of the softmaxes
 // over its parts.
 //
-// CTA layout: 4 consumer warps + 1 producer warp.  The producer streams the
-// partition's (block, KV head) tiles into a ring with TMA exactly as the
-// decode kernel does; every consumer warp reads every stage.  Consumer warp
-// w owns query rows 16w .. 16w+15 of the CTA's row tile (row r = member
-// r / G, head r % G of that member's KV head) and runs the decode warp core
-// (decode_common.cuh) over them: S^T = K Q^T with the 16 rows as the N
-// dimension, online softmax, O^T += V^T P^T.  A member whose shared prefix
-// ends before a block masks its columns for that block.
+// With up to 64 query rows per shared tile this is a dense contraction, so
+// both products run as tcgen05.mma.kind::f16 with fp32 accumulators in
+// tensor memory (TMEM), M = 128 rows:
+//   S = Q K^T   A = Q [128 rows x 128 dims], B = K [64 tokens x 128 dims],
+//               both K-major, 128-byte swizzle      -> TMEM columns [0, 64) or [64, 128)
+//   O += P V    A = P [128 rows x 64 tokens] (K-major), B = V [64 tokens x
+//               128 dims] read dims-major (MN-major), 16 tokens per product
+//               (within one block)                   -> TMEM columns [128, 256)
+// The tile's 64 query rows are fed twice as Q (rows r and r + 64 of A), so
+// TMEM lanes r and r + 64 hold the same row of S: thread r takes the first
+// 32 tokens of each chunk, thread r + 64 the other 32, and the two exchange
+// their maxima and sums.  P keeps ~16 significant bits as a 16-bit high part
+// plus a 16-bit residual: row r of P's A operand is the high part of query
+// row r and row r + 64 its residual, so one product accumulates both, in
+// lanes r and r + 64 of O, which the epilogue adds.  (A tcgen05.mma with
+// M = 128 costs about the same for any N up to 128, so the rows a product
+// carries matter more than its width.)
+//
+// The partition streams through in chunks of 64 tokens, pipelined across
+// three roles that hand off on mbarriers:
+//   TMA warp: the chunk's (block, KV head) tiles of K and V into a 4-stage
+//     ring.  K lands as two [64 tokens][64 dims] halves, tokens contiguous
+//     across the chunk's blocks (one copy per block and half); V lands tile
+//     after tile, each as its two [BS][64] halves (one copy per tile).  The
+//     copies of a chunk are issued from separate lanes;
+//   MMA warp (one thread): S(c+1) = Q K(c+1)^T into the other S buffer while
+//     the softmax works on chunk c, then O += P(c) V(c) once P(c) is written;
+//     each product's completion is signalled by tcgen05.commit;
+//   softmax warps 0-3 (TMEM lanes 0-127): S(c) from TMEM, the online softmax
+//     in the log2 domain with the running max raised lazily (as in the decode
+//     warp core; O and l are rescaled when it is), P(c) into one of two
+//     shared-memory buffers, and at the end the normalised output and
+//     log-sum-exp.  A chunk's softmax waits for the previous chunk's product
+//     only when it has to rescale O.
+// Every wait is bounded; a wait that runs out records PKV_DEVERR_TIMEOUT,
+// the roles stop at the same chunk, and the copies and products already
+// issued are waited for before the CTA frees its tensor memory.
 #include "decode_common.cuh"
 
 namespace pkv {
 
-constexpr int kPrefixWarps = kPrefixRows / 16;  // consumer warps
+constexpr int kSoftWarps = 4;             // TMEM lanes 0-127
+constexpr int kTmaWarp = kSoftWarps;      // K/V loads
+constexpr int kMmaWarp = kSoftWarps + 1;  // tensor-core products (lane 0)
+constexpr int kPrefixThreads = (kSoftWarps + 2) * 32;
+constexpr int kChunk = 64;                // tokens per pipeline step
+constexpr int kUmmaM = 128;               // M of both products
+constexpr int kRing = 4;                  // K/V chunks in flight
+constexpr uint32_t kTmemCols = 256;       // S: [0, 64) and [64, 128); O: [128, 256)
+constexpr uint32_t kOCol = 128;
 
-#ifndef PKV_PNST16
-#define PKV_PNST16 8
-#endif
-#ifndef PKV_PNST32
-#define PKV_PNST32 4
-#endif
+// ---- tcgen05 wrappers (PTX ISA: tcgen05 instructions, shared memory and
+// instruction descriptors)
 
-template <int BS, int NST>
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand: start
+// address, leading- and stride-dimension byte offsets (all in 16-byte
+// units), the fixed 0b001 at bits 46-48, swizzle mode 2 (128 B) at 61-63.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulate, A and B both bf16 or
+// both fp16, operand majorness, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__device__ __forceinline__ uint32_t umma_idesc(bool bf16, int M, int N, bool a_mn_major, bool b_mn_major) {
+    const uint32_t t = bf16 ? 1u : 0u;
+    return (1u << 4) | (t << 7) | (t << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D (TMEM) = A B^T (+ D when accumulate); issued by one thread.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, int accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05.mma this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {  // whole warp
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(cols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {  // whole warp
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
+// 32w .. 32w+31); every lane of the warp executes it.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// The reverse: 32 fp32 columns of this thread's lane from registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Barrier over the softmax warps only (named barrier 1).
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftWarps * 32) : "memory"); }
+
+// Byte offset of 16-byte chunk c (0-7) of row r in a [rows][64 x 16-bit]
+// region with the 128-byte swizzle (the layout TMA writes and the
+// descriptors above read).
+__device__ __forceinline__ uint32_t sw128_chunk(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
 struct PrefixSmem {
-    static constexpr int kTileBytes = BS * kHeadDim * 2;
-    static constexpr int kHalfBytes = kTileBytes / 2;
-    static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStagesBytes = NST * kStageBytes;
-    // epilogue: the rows' outputs [64][kRedStride] and (m, l) [64][2]
-    static constexpr int kRedBytes = kPrefixRows * kRedStride * 4 + kPrefixRows * 2 * 4;
-    static constexpr int kRingBytes = ((kStagesBytes > kRedBytes ? kStagesBytes : kRedBytes) + 1023) / 1024 * 1024;
-    static constexpr int kBarOffset = kRingBytes;
+    static constexpr int kQHalf = kUmmaM * 128;   // Q: [128 rows][64 dims] per dims half, 16 KiB
+    static constexpr int kKVHalf = kChunk * 128;  // a chunk of K or V: [64 tokens][64 dims] per dims half, 8 KiB
+    static constexpr int kPBuf = kUmmaM * 128;    // P: [128 rows][64 tokens], 16 KiB; two buffers
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQOff + 2 * kQHalf;
+    static constexpr int kVOff = kKOff + kRing * 2 * kKVHalf;
+    static constexpr int kPOff = kVOff + kRing * 2 * kKVHalf;
+    static constexpr int kBarOff = kPOff + 2 * kPBuf;
+    // kvfull[kRing], kvempty[kRing], sfull[2], sfree[2], pfull[2], pvdone[2]
+    static constexpr int kNumBars = 2 * kRing + 8;
+    static constexpr int kSlotOff = kBarOff + kNumBars * 8;
     // per member of the tile: sequence, prefix tokens (0 when it takes no
     // part), partitions in all, whether the prefix side merges; per (member,
     // head tile): merge verdict
-    static constexpr int kMemOffset = kBarOffset + 2 * NST * 8;
+    static constexpr int kMemOff = kSlotOff + 16;
     static constexpr int kMemBytes = kPrefixRows * 4 * 4 + kPrefixRows * 4 * 4;
-    static constexpr int kFlagOffset = kMemOffset + kMemBytes;
-    static constexpr int kTotal = kFlagOffset + 16;
-    static constexpr int kDynamic = kTotal + 1024;
+    static constexpr int kXchOff = kMemOff + kMemBytes;  // [2][128] chunk maxima, [128] row sums
+    static constexpr int kFlagOff = kXchOff + 3 * kUmmaM * 4;
+    static constexpr int kTotal = kFlagOff + 16;
+    static constexpr int kDynamic = kTotal + 1024;  // slack to align the base to 1024 B
+    // epilogue: every lane's O row, [128][kRedStride] floats over the K/V ring
+    static constexpr int kRedOff = kKOff;
+    static_assert(kUmmaM * kRedStride * 4 <= 2 * kRing * 2 * kKVHalf, "O rows fit the ring");
 };
 
-template <bool kBF16, int BS, int NST>
-__global__ void __launch_bounds__((kPrefixWarps + 1) * 32, 2)
+template <bool kBF16, int BS>
+__global__ void __launch_bounds__(kPrefixThreads, 1)
     group_prefix_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         const DecodeParams p) {
-    using S = PrefixSmem<BS, NST>;
+    using S = PrefixSmem;
     constexpr int D = kHeadDim;
-    constexpr int NH = 2;  // 16 rows per consumer warp
+    constexpr int kBlocksPerChunk = kChunk / BS;
+    static_assert(kChunk % BS == 0 && 3 * kBlocksPerChunk <= 32, "whole blocks per chunk, one copy per lane");
+    static_assert(2 * kPrefixRows == kUmmaM && kSoftWarps * 32 == kUmmaM, "each row twice, one thread per TMEM lane");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_sa = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + (((raw_sa + 1023u) & ~1023u) - raw_sa);
@@ -74,20 +205,27 @@ __global__ void __launch_bounds__((kPrefixWarps + 1) * 32, 2)
     const int G = p.group;
 
     pdl_launch_dependents();
-    if (tid == 32 * kPrefixWarps) {
+    if (tid == 32 * kTmaWarp) {
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
     }
     pdl_wait();
 
-    int* mem_s = reinterpret_cast<int*>(smem + S::kMemOffset);  // [64]
-    int* mem_lim = mem_s + kPrefixRows;                         // [64]
-    int* mem_np = mem_lim + kPrefixRows;                        // [64] partitions in all
-    int* mem_arrive = mem_np + kPrefixRows;                     // [64] 1: the prefix side merges
-    int* verdict = mem_arrive + kPrefixRows;                    // [64 * 4]
-    int* flags = reinterpret_cast<int*>(smem + S::kFlagOffset); // [0]: bad block / timeout, [1]: tile token end
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOffset);
-    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + NST);
+    int* mem_s = reinterpret_cast<int*>(smem + S::kMemOff);   // [64]
+    int* mem_lim = mem_s + kPrefixRows;                       // [64]
+    int* mem_np = mem_lim + kPrefixRows;                      // [64] partitions in all
+    int* mem_arrive = mem_np + kPrefixRows;                   // [64] 1: the prefix side merges
+    int* verdict = mem_arrive + kPrefixRows;                  // [64 * 4]
+    // [0]: bad block id (bit 0) / a wait ran out (bit 1); [1]: tile token
+    // end; [2]: a softmax warp's wait ran out (read only after softmax_sync)
+    int* flags = reinterpret_cast<int*>(smem + S::kFlagOff);
+    float* xch = reinterpret_cast<float*>(smem + S::kXchOff);
+    const uint32_t bar0 = smem_addr(smem + S::kBarOff);
+    const uint32_t kvfull0 = bar0, kvempty0 = bar0 + 8 * kRing, sfull0 = bar0 + 16 * kRing, sfree0 = sfull0 + 16,
+                   pfull0 = sfree0 + 16, pvdone0 = pfull0 + 16;
+    const uint32_t slot = smem_addr(smem + S::kSlotOff);
+    uint8_t* const qreg = smem + S::kQOff;
+    uint8_t* const preg = smem + S::kPOff;
 
     const int gs0 = p.group_starts[g], gs1 = p.group_starts[g + 1];
     const bool bad_group = gs0 < 0 || gs1 < gs0 || gs1 > p.num_seqs;
@@ -103,9 +241,18 @@ __global__ void __launch_bounds__((kPrefixWarps + 1) * 32, 2)
             record_error(p.err, PKV_DEVERR_GROUP);
         flags[0] = 0;
         flags[1] = 0;
-        for (int i = 0; i < NST; ++i) {
-            mbar_init(full0 + 8 * i, 1);
-            mbar_init(empty0 + 8 * i, kPrefixWarps);
+        flags[2] = 0;
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(kvfull0 + 8 * i, 1);
+            mbar_init(kvempty0 + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(sfull0 + 8 * i, 1);
+            mbar_init(sfree0 + 8 * i, kSoftWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(pfull0 + 8 * i, kSoftWarps);
+            mbar_init(pvdone0 + 8 * i, 1);
         }
         fence_barrier_init();
     }
@@ -127,146 +274,318 @@ __global__ void __launch_bounds__((kPrefixWarps + 1) * 32, 2)
     __syncthreads();
     const int tok1 = flags[1];
     if (tok1 <= tok0) return;  // no member's prefix reaches this partition
-    const int nblk = (tok1 - tok0) / BS;  // prefix lengths are whole blocks
-    const int blk0 = tok0 / BS;
+    const int ntok = tok1 - tok0;  // whole blocks (prefix lengths are)
+    const int nchunks = (ntok + kChunk - 1) / kChunk;
+    const int rows = nmem * G;  // <= 64
 
-    WarpAcc<NH> acc;
-    acc_reset(acc);
-    int issued = 0;
+    // ---- TMEM (MMA warp), Q rows into shared memory (softmax warps)
+    if (warp == kMmaWarp) tmem_alloc(slot, kTmemCols);
+    if (warp < kSoftWarps) {
+        // Q rows of the tile (row r: member r / G, head r % G of its KV head),
+        // zeros up to row 63, and again as rows 64-127.
+        for (int i = tid; i < kPrefixRows * 16; i += kSoftWarps * 32) {
+            const int r = i >> 4, c = i & 15;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r < rows) {
+                const int mi = r / G;
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    static_cast<const uint16_t*>(p.q) + ((int64_t)mem_s[mi] * p.num_q_heads + kvh * G + r - mi * G) * D);
+                v = __ldg(src + c);
+            }
+            *reinterpret_cast<uint4*>(qreg + (c >> 3) * S::kQHalf + sw128_chunk(r, c & 7)) = v;
+            *reinterpret_cast<uint4*>(qreg + (c >> 3) * S::kQHalf + sw128_chunk(r + kPrefixRows, c & 7)) = v;
+        }
+        fence_proxy_async_shared();  // the tensor cores read Q through the async proxy
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kSlotOff);
 
-    if (warp == kPrefixWarps) {
-        // ------------------------------------------------------------ producer
+    float m_run = -INFINITY;  // softmax threads: running max of the row (raised lazily)
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ K/V loads
         const uint64_t policy = l2_policy_evict_first();
-        const int32_t* table = p.block_tables + (int64_t)gs0 * p.max_blocks_per_seq + blk0;
-        bool ok = true;
-        for (int c = 0; c < nblk; c += 32) {
-            const int j = c + lane;
+        const int32_t* table = p.block_tables + (int64_t)gs0 * p.max_blocks_per_seq + tok0 / BS;
+        const int nblk = ntok / BS;
+        int issued = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c % kRing;
+            const int b0 = c * kBlocksPerChunk, nb = min(kBlocksPerChunk, nblk - b0);
             int id = 0;
             bool bad = false;
-            if (j < nblk) {
-                id = __ldg(table + j);
+            if (lane < nb) {
+                id = __ldg(table + b0 + lane);
                 bad = id < 0 || (int64_t)id >= p.num_blocks;
-                if (bad) id = 0;
+                if (bad) id = 0;  // keep the shape; the outputs are zeroed later
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) {
                 atomicOr(flags, 1);
                 record_error(p.err, PKV_DEVERR_BLOCK_ID);
             }
-            const int n = min(32, nblk - c);
-            for (int i = 0; i < n; ++i) {
-                const int pid = __shfl_sync(0xffffffffu, id, i);
-                if (lane == 0 && ok) {
-                    const int jj = c + i, st = jj % NST, round = jj / NST;
-                    if (round > 0) ok = mbar_wait(empty0 + 8 * st, (round - 1) & 1);
-                    if (ok) {
-                        const uint32_t fb = full0 + 8 * st;
-                        mbar_arrive_expect_tx(fb, S::kStageBytes);
-                        const uint32_t dst = smem_addr(smem + st * S::kStageBytes);
-                        const int y = (pid * p.num_kv_heads + kvh) * BS;
-                        tma_load_2d(dst, &tmk, fb, 0, y, policy);
-                        tma_load_2d(dst + S::kHalfBytes, &tmk, fb, 64, y, policy);
-                        tma_load_2d(dst + S::kTileBytes, &tmv, fb, 0, y, policy);
-                        tma_load_2d(dst + S::kTileBytes + S::kHalfBytes, &tmv, fb, 64, y, policy);
-                        ++issued;
-                    } else {
-                        atomicOr(flags, 2);
-                        record_error(p.err, PKV_DEVERR_TIMEOUT);
-                    }
-                }
-                __syncwarp();
-            }
-        }
-    } else {
-        // ------------------------------------------------------------ consumers
-        // rows of this warp: 16 warp + 8 n + (lane / 4) for the Q operand,
-        // columns 16 warp + 8 n + 2 (lane % 4) + c for the scores it holds
-        const int gq = lane >> 2, t = lane & 3;
-        QFrag<NH> qf;
-#pragma unroll
-        for (int n = 0; n < NH; ++n) {
-            const int r = 16 * warp + 8 * n + gq, mi = r / G;
-            const uint32_t* qr =
-                mi < nmem ? reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(p.q) +
-                                                              ((int64_t)mem_s[mi] * p.num_q_heads + kvh * G + r - mi * G) *
-                                                                  kHeadDim)
-                          : nullptr;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                qf.b[n][ks][0] = qr ? __ldg(qr + 8 * ks + t) : 0u;
-                qf.b[n][ks][1] = qr ? __ldg(qr + 8 * ks + 4 + t) : 0u;
-            }
-        }
-        int lim[NH][2];  // prefix tokens of each held column's member (0: none)
-#pragma unroll
-        for (int n = 0; n < NH; ++n)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int mi = (16 * warp + 8 * n + 2 * t + c) / G;
-                lim[n][c] = mi < nmem ? mem_lim[mi] : 0;
-            }
-        const float sl2 = p.scale_log2;
-        for (int jj = 0; jj < nblk; ++jj) {
-            const int st = jj % NST, round = jj / NST;
-            if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * st, round & 1))) {
+            bool ok = true;
+            if (lane == 0 && c >= kRing) ok = mbar_wait(kvempty0 + 8 * st, ((c / kRing) - 1) & 1);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
                 if (lane == 0) {
                     atomicOr(flags, 2);
                     record_error(p.err, PKV_DEVERR_TIMEOUT);
                 }
                 break;
             }
-            const int tb = tok0 + jj * BS;
-            uint32_t cols = 0;
-#pragma unroll
-            for (int n = 0; n < NH; ++n)
-#pragma unroll
-                for (int c = 0; c < 2; ++c) cols |= (tb < lim[n][c] ? 1u : 0u) << (2 * n + c);
-            const uint32_t kb = smem_addr(smem + st * S::kStageBytes);
-            attend_block<kBF16, BS, NH, true, true>(acc, qf, kb, kb + S::kTileBytes, BS, sl2, lane, cols);
+            const uint32_t fb = kvfull0 + 8 * st;
+            const uint32_t kdst = smem_addr(smem + S::kKOff + st * 2 * S::kKVHalf);
+            const uint32_t vdst = smem_addr(smem + S::kVOff + st * 2 * S::kKVHalf);
+            if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)nb * BS * 128 * 4);
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * st);
+            // one copy per lane, so that the copies of a chunk are issued side
+            // by side: lane 3b + w takes block b's K dims half w (w < 2; the
+            // chunk's tokens stay contiguous within each half) or its whole
+            // V tile (w = 2; the tile's two halves back to back)
+            {
+                const int b = lane / 3, w = lane - 3 * b;
+                const int pid = __shfl_sync(0xffffffffu, id, b & 31);
+                if (b < nb) {
+                    const int y = (pid * p.num_kv_heads + kvh) * BS;  // row of the tile in [rows][128]
+                    if (w < 2)
+                        tma_load_2d(kdst + w * S::kKVHalf + b * BS * 128, &tmk, fb, 64 * w, y, policy);
+                    else
+                        tma_load_3d(vdst + b * 2 * BS * 128, &tmv, fb, 0, y, 0, policy);
+                }
+            }
+            ++issued;
         }
-        acc_finish(acc);
+        // every copy issued has landed before the ring is reused or freed
+        // (already true when the products consumed them; bounded otherwise)
+        if (lane == 0)
+            for (int st = 0; st < kRing && st < issued; ++st)
+                mbar_wait(kvfull0 + 8 * st, ((st + kRing * ((issued - 1 - st) / kRing)) / kRing) & 1);
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ products
+        if (lane == 0) {
+            const uint32_t id_o = umma_idesc(kBF16, kUmmaM, D, false, true);
+            uint32_t last_bar = 0, last_par = 0;  // the latest commit and its phase parity
+            bool ok = true;
+            for (int c = -1; c < nchunks && ok; ++c) {
+                // S(c+1) = Q K(c+1)^T into S buffer (c+1) & 1, ahead of the softmax
+                const int cs = c + 1;
+                if (cs < nchunks) {
+                    const int st = cs % kRing, sb = cs & 1;
+                    ok = mbar_wait(kvfull0 + 8 * st, (cs / kRing) & 1) &&
+                         (cs < 2 || mbar_wait(sfree0 + 8 * sb, ((cs >> 1) - 1) & 1));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t kb = smem_addr(smem + S::kKOff + st * 2 * S::kKVHalf);
+                    const int nt = min(kChunk, ntok - cs * kChunk);  // a multiple of 16
+                    const uint32_t id_s = umma_idesc(kBF16, kUmmaM, nt, false, false);
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t a = smem_addr(qreg + (ks >> 2) * S::kQHalf) + (ks & 3) * 32;
+                        const uint32_t b = kb + (ks >> 2) * S::kKVHalf + (ks & 3) * 32;
+                        umma_f16(tmem + sb * kChunk, umma_desc_sw128(a, 16, 1024), umma_desc_sw128(b, 16, 1024),
+                                 id_s, ks > 0);
+                    }
+                    umma_commit(sfull0 + 8 * sb);
+                    last_bar = sfull0 + 8 * sb;
+                    last_par = (cs >> 1) & 1;
+                }
+                if (c < 0) continue;
+                // O += P(c) V(c): rows 0-63 the high part, rows 64-127 the residual
+                const int pb = c & 1;
+                ok = mbar_wait(pfull0 + 8 * pb, (c >> 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const int st = c % kRing;
+                const uint32_t vb = smem_addr(smem + S::kVOff + st * 2 * S::kKVHalf);
+                const uint32_t pa = smem_addr(preg + pb * S::kPBuf);
+                const int nk = min(kChunk, ntok - c * kChunk) / 16;
+                // V's tiles lie block after block, each as its two dims halves
+                // ([BS][64] apiece): 16 tokens start at row 16 ks of the chunk
+                for (int ks = 0; ks < nk; ++ks) {
+                    const uint32_t v0 = vb + (16 * ks / BS) * (2 * BS * 128) + (16 * ks % BS) * 128;
+                    umma_f16(tmem + kOCol, umma_desc_sw128(pa + ks * 32, 16, 1024),
+                             umma_desc_sw128(v0, BS * 128, 1024), id_o, c > 0 || ks > 0);
+                }
+                umma_commit(kvempty0 + 8 * st);
+                umma_commit(pvdone0 + 8 * pb);
+                last_bar = pvdone0 + 8 * pb;
+                last_par = (c >> 1) & 1;
+            }
+            if (!ok) {
+                atomicOr(flags, 2);
+                record_error(p.err, PKV_DEVERR_TIMEOUT);
+            }
+            // every product issued has completed before TMEM is read or freed
+            if (last_bar) mbar_wait(last_bar, last_par);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int r = tid & (kPrefixRows - 1);  // the tile row this thread works on
+        const int half = tid >> 6;              // 0: tokens 0-31 of a chunk, dims 0-63; 1: the rest
+        const int lim = r < rows ? min(ntok, mem_lim[r / G] - tok0) : 0;  // tokens row r attends (<= 0: none)
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+        const float sl2 = p.scale_log2;
+        float l = 0.f;  // this half's share of the row sum
+        bool ok = true;
+        // Wait for the product of chunk j (warp-uniform verdict).
+        auto pv_done = [&](int j) { return __all_sync(0xffffffffu, mbar_wait(pvdone0 + 8 * (j & 1), (j >> 1) & 1)); };
+        for (int c = 0; c < nchunks; ++c) {
+            const int sb = c & 1;
+            float v[32];
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(sfull0 + 8 * sb, (c >> 1) & 1));
+            if (ok) {
+                tc_fence_after();
+                tmem_ld32(lane_addr + sb * kChunk + 32 * half, v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sfree0 + 8 * sb);
+            }
+            if (!ok && lane == 0) flags[2] = 1;
+            const int t0 = c * kChunk + 32 * half;  // partition token of v[0]
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                v[j] = ok && t0 + j < lim ? v[j] * sl2 : -INFINITY;
+                mx = fmaxf(mx, v[j]);
+            }
+            float* xm = xch + sb * kUmmaM;
+            xm[tid] = mx;
+            softmax_sync();
+            if (flags[2]) {  // every softmax thread sees the same verdict here
+                ok = false;
+                break;
+            }
+            mx = fmaxf(mx, xm[tid ^ kPrefixRows]);
+            // raise m only when a score exceeds it by more than kLazyMargin;
+            // both threads of a row take the same decision
+            const bool raise = mx > m_run + kLazyMargin;
+            float alpha = 1.f;
+            if (raise) {
+                alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - mx);
+                m_run = mx;
+            }
+            const float ms = m_run == -INFINITY ? 0.f : m_run;
+            l *= alpha;
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float p0 = exp2f(v[2 * e] - ms), p1 = exp2f(v[2 * e + 1] - ms);
+                l += p0 + p1;
+                float r0, r1;
+                hi[e] = pack2<kBF16>(p0, p1, r0, r1);
+                lo[e] = pack2<kBF16>(p0 - r0, p1 - r1);
+            }
+            // O is rescaled once the previous chunk's product is in it; the P
+            // buffer is reused once the product two chunks back has read it
+            const bool rescale = c > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+            if (rescale)
+                ok = pv_done(c - 1);
+            else if (c >= 2)
+                ok = pv_done(c - 2);
+            if (!ok) {
+                if (lane == 0) flags[2] = 1;  // the next softmax_sync stops every softmax warp
+                continue;
+            }
+            tc_fence_after();
+            if (rescale) {
+                // this lane's row of O (the high or the residual product)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float o[32];
+                    const uint32_t oa = lane_addr + kOCol + 32 * q;
+                    tmem_ld32(oa, o);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] *= alpha;
+                    tmem_st32(oa, o);
+                }
+            }
+            // tokens 32 half .. +31 (16-byte chunks 4 half .. +3): the high
+            // part into row r, the residual into row r + 64
+            uint8_t* pbuf = preg + sb * S::kPBuf;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int cc = 4 * half + q;
+                *reinterpret_cast<uint4*>(pbuf + sw128_chunk(r, cc)) =
+                    make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+                *reinterpret_cast<uint4*>(pbuf + sw128_chunk(r + kPrefixRows, cc)) =
+                    make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+            }
+            fence_proxy_async_shared();  // the tensor cores read P through the async proxy
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pfull0 + 8 * sb);
+        }
+        if (ok) ok = pv_done(nchunks - 1);
+        tc_fence_after();
+        if (!ok && lane == 0) {
+            atomicOr(flags, 2);
+            record_error(p.err, PKV_DEVERR_TIMEOUT);
+        }
+        xch[2 * kUmmaM + tid] = l;  // the row sum's halves, combined below
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
 
     const int fl = flags[0];
-    if ((fl & 2) && warp == kPrefixWarps && lane == 0) {
-        for (int st = 0; st < NST && st < issued; ++st) {
-            const int last_round = (issued - 1 - st) / NST;
-            mbar_wait(full0 + 8 * st, last_round & 1);
+    float* red = reinterpret_cast<float*>(smem + S::kRedOff);  // [128 lanes][kRedStride]
+    if (warp < kSoftWarps) {
+        // every lane's O row into shared memory (the ring is idle now; the
+        // TMEM loads are warp-collective, so every lane runs them)
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float v[32];
+            if (!(fl & 2)) {
+                tmem_ld32(lane_addr + kOCol + 32 * q, v);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(red + tid * kRedStride + 32 * q + j) =
+                    make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
     }
     __syncthreads();
-
-    // ---- each warp's 16 rows are complete: stage them, then write them out
-    float* red = reinterpret_cast<float*>(smem);  // [64][kRedStride]
-    float* ml = red + kPrefixRows * kRedStride;    // [64][2]
-    if (warp < kPrefixWarps) acc_to_smem(acc, red + 16 * warp * kRedStride, ml + 16 * warp * 2, 0, 16, lane);
-    __syncthreads();
-
-    const bool bad = fl != 0;
-    const int rows = nmem * G;
-    for (int i = tid; i < rows * (D / 4); i += blockDim.x) {
-        const int r = i / (D / 4), c4 = i - r * (D / 4);
-        const int mi = r / G;
-        if (tok0 >= mem_lim[mi]) continue;  // this member's prefix ends before the partition
-        const int s = mem_s[mi], h = kvh * G + r - mi * G;
-        const float l = ml[r * 2 + 1];
-        const float inv = 1.f / l;
-        const float* src = red + r * kRedStride + 4 * c4;
-        float4 o = make_float4(src[0] * inv, src[1] * inv, src[2] * inv, src[3] * inv);
-        if (bad) o = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (mem_np[mi] > 1) {
+    if (warp < kSoftWarps) {
+        // each row's normalised output (high + residual product) and
+        // log-sum-exp; thread r writes dims 0-63 of row r, thread r + 64 dims 64-127
+        const int r = tid & (kPrefixRows - 1), half = tid >> 6, mi = r / G;
+        const bool has = r < rows && tok0 < mem_lim[mi];  // row r's member has prefix tokens here
+        if (has) {
+            const bool bad = fl != 0;
+            const int s = mem_s[mi], h = kvh * G + r - mi * G;
+            const bool partial = mem_np[mi] > 1;
             const int64_t idx = ((int64_t)s * p.num_q_heads + h) * p.max_parts + part;
-            reinterpret_cast<float4*>(p.part_o + idx * D)[c4] = o;
-            if (c4 == 0) p.part_lse[idx] = bad ? INFINITY : ml[r * 2] + log2f(l);
-        } else {
-            store_out(p, s, h, 4 * c4, o.x);
-            store_out(p, s, h, 4 * c4 + 1, o.y);
-            store_out(p, s, h, 4 * c4 + 2, o.z);
-            store_out(p, s, h, 4 * c4 + 3, o.w);
+            const float lsum = xch[2 * kUmmaM + r] + xch[2 * kUmmaM + r + kPrefixRows];
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            const float* hi_row = red + r * kRedStride + 64 * half;
+            const float* lo_row = red + (r + kPrefixRows) * kRedStride + 64 * half;
+            for (int j = 0; j < 64; j += 4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(hi_row + j);
+                const float4 b4 = *reinterpret_cast<const float4*>(lo_row + j);
+                float4 o = make_float4((a4.x + b4.x) * inv, (a4.y + b4.y) * inv, (a4.z + b4.z) * inv,
+                                       (a4.w + b4.w) * inv);
+                if (bad) o = make_float4(0.f, 0.f, 0.f, 0.f);
+                const int d = 64 * half + j;
+                if (partial) {
+                    *reinterpret_cast<float4*>(p.part_o + idx * D + d) = o;
+                } else {
+                    store_out(p, s, h, d, o.x);
+                    store_out(p, s, h, d + 1, o.y);
+                    store_out(p, s, h, d + 2, o.z);
+                    store_out(p, s, h, d + 3, o.w);
+                }
+            }
+            if (partial && half == 0) p.part_lse[idx] = bad ? INFINITY : m_run + log2f(lsum);
         }
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 
     if (p.fuse_merge) {
         // One arrival per (member, head tile of the decode kernel) that takes
@@ -290,7 +609,7 @@ __global__ void __launch_bounds__((kPrefixWarps + 1) * 32, 2)
             const int mi = u / p.head_tiles, ht = u - mi * p.head_tiles;
             __threadfence();
             merge_row_partials(p, mem_s[mi], kvh * G + ht * HT, min(HT, G - ht * HT), mem_np[mi],
-                               reinterpret_cast<float*>(smem));
+                               reinterpret_cast<float*>(smem));  // Q's region: free now
             __syncthreads();  // the scratch is reused by the next merge
         }
     }
@@ -299,13 +618,12 @@ __global__ void __launch_bounds__((kPrefixWarps + 1) * 32, 2)
 template <bool kBF16, int BS>
 static cudaError_t launch_prefix_t(const DecodeParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
                                    cudaStream_t stream, int* launches) {
-    constexpr int NST = BS == 16 ? PKV_PNST16 : PKV_PNST32;
-    using S = PrefixSmem<BS, NST>;
-    auto kern = group_prefix_kernel<kBF16, BS, NST>;
+    using S = PrefixSmem;
+    auto kern = group_prefix_kernel<kBF16, BS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kDynamic);
     if (e != cudaSuccess) return e;
     const dim3 grid(p.prefix_parts, p.num_kv_heads * p.row_tiles, p.num_groups);
-    e = launch_pdl(kern, grid, dim3((kPrefixWarps + 1) * 32), S::kDynamic, stream, tmk, tmv, p);
+    e = launch_pdl(kern, grid, dim3(kPrefixThreads), S::kDynamic, stream, tmk, tmv, p);
     if (e == cudaSuccess) ++*launches;
     return e;
 }
