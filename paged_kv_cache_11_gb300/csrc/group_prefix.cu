@@ -194,6 +194,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     constexpr int kBlocksPerChunk = kChunk / BS;
     static_assert(kChunk % BS == 0 && 3 * kBlocksPerChunk <= 32, "whole blocks per chunk, one copy per lane");
     static_assert(2 * kPrefixRows == kUmmaM && kSoftWarps * 32 == kUmmaM, "each row twice, one thread per TMEM lane");
+    static_assert(kPrefixRows * 16 % (kSoftWarps * 32) == 0, "whole Q loads per thread");
+    static_assert(kPrefixPartitionMax / 16 <= 64, "a partition's block ids fit two registers per lane");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_sa = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + (((raw_sa + 1023u) & ~1023u) - raw_sa);
@@ -217,7 +219,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     int* mem_arrive = mem_np + kPrefixRows;                   // [64] 1: the prefix side merges
     int* verdict = mem_arrive + kPrefixRows;                  // [64 * 4]
     // [0]: bad block id (bit 0) / a wait ran out (bit 1); [1]: tile token
-    // end; [2]: a softmax warp's wait ran out (read only after softmax_sync)
+    // end; [2]: a softmax warp's wait ran out (read only after softmax_sync);
+    // [3]: some member's partials are merged on this side
     int* flags = reinterpret_cast<int*>(smem + S::kFlagOff);
     float* xch = reinterpret_cast<float*>(smem + S::kXchOff);
     const uint32_t bar0 = smem_addr(smem + S::kBarOff);
@@ -242,6 +245,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         flags[0] = 0;
         flags[1] = 0;
         flags[2] = 0;
+        flags[3] = 0;
         for (int i = 0; i < kRing; ++i) {
             mbar_init(kvfull0 + 8 * i, 1);
             mbar_init(kvempty0 + 8 * i, 1);
@@ -270,6 +274,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         // (with one, the decode kernel folds them in; with more, it merges)
         mem_arrive[i] = sp.nsuf == 0 ? 1 : 0;
         if (!sp.err && sp.plen > tok0) atomicMax(flags + 1, min(sp.plen, tok0 + p.prefix_partition));
+        if (sp.nsuf == 0 && sp.npre > 1 && sp.plen > tok0) flags[3] = 1;  // some row merges here
     }
     __syncthreads();
     const int tok1 = flags[1];
@@ -282,18 +287,26 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     if (warp == kMmaWarp) tmem_alloc(slot, kTmemCols);
     if (warp < kSoftWarps) {
         // Q rows of the tile (row r: member r / G, head r % G of its KV head),
-        // zeros up to row 63, and again as rows 64-127.
-        for (int i = tid; i < kPrefixRows * 16; i += kSoftWarps * 32) {
-            const int r = i >> 4, c = i & 15;
-            uint4 v = make_uint4(0, 0, 0, 0);
+        // zeros up to row 63, and again as rows 64-127.  Every load is
+        // issued before any is stored.
+        constexpr int kQPerThread = kPrefixRows * 16 / (kSoftWarps * 32);
+        uint4 qv[kQPerThread];
+#pragma unroll
+        for (int k = 0; k < kQPerThread; ++k) {
+            const int i = tid + k * kSoftWarps * 32, r = i >> 4, c = i & 15;
+            qv[k] = make_uint4(0, 0, 0, 0);
             if (r < rows) {
                 const int mi = r / G;
                 const uint4* src = reinterpret_cast<const uint4*>(
                     static_cast<const uint16_t*>(p.q) + ((int64_t)mem_s[mi] * p.num_q_heads + kvh * G + r - mi * G) * D);
-                v = __ldg(src + c);
+                qv[k] = __ldg(src + c);
             }
-            *reinterpret_cast<uint4*>(qreg + (c >> 3) * S::kQHalf + sw128_chunk(r, c & 7)) = v;
-            *reinterpret_cast<uint4*>(qreg + (c >> 3) * S::kQHalf + sw128_chunk(r + kPrefixRows, c & 7)) = v;
+        }
+#pragma unroll
+        for (int k = 0; k < kQPerThread; ++k) {
+            const int i = tid + k * kSoftWarps * 32, r = i >> 4, c = i & 15;
+            *reinterpret_cast<uint4*>(qreg + (c >> 3) * S::kQHalf + sw128_chunk(r, c & 7)) = qv[k];
+            *reinterpret_cast<uint4*>(qreg + (c >> 3) * S::kQHalf + sw128_chunk(r + kPrefixRows, c & 7)) = qv[k];
         }
         fence_proxy_async_shared();  // the tensor cores read Q through the async proxy
     }
@@ -308,22 +321,27 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         // ------------------------------------------------------------ K/V loads
         const uint64_t policy = l2_policy_evict_first();
         const int32_t* table = p.block_tables + (int64_t)gs0 * p.max_blocks_per_seq + tok0 / BS;
-        const int nblk = ntok / BS;
+        const int nblk = ntok / BS;  // <= kPrefixPartitionMax / 16 = 64
+        // the partition's block ids, loaded once: block j in ids[j / 32] of lane j % 32
+        int ids[2];
+        bool bad = false;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int j = 32 * k + lane;
+            ids[k] = j < nblk ? __ldg(table + j) : 0;
+            if (ids[k] < 0 || (int64_t)ids[k] >= p.num_blocks) {
+                bad = true;
+                ids[k] = 0;  // keep the shape; the outputs are zeroed later
+            }
+        }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) {
+            atomicOr(flags, 1);
+            record_error(p.err, PKV_DEVERR_BLOCK_ID);
+        }
         int issued = 0;
         for (int c = 0; c < nchunks; ++c) {
             const int st = c % kRing;
             const int b0 = c * kBlocksPerChunk, nb = min(kBlocksPerChunk, nblk - b0);
-            int id = 0;
-            bool bad = false;
-            if (lane < nb) {
-                id = __ldg(table + b0 + lane);
-                bad = id < 0 || (int64_t)id >= p.num_blocks;
-                if (bad) id = 0;  // keep the shape; the outputs are zeroed later
-            }
-            if (__any_sync(0xffffffffu, bad) && lane == 0) {
-                atomicOr(flags, 1);
-                record_error(p.err, PKV_DEVERR_BLOCK_ID);
-            }
             bool ok = true;
             if (lane == 0 && c >= kRing) ok = mbar_wait(kvempty0 + 8 * st, ((c / kRing) - 1) & 1);
             if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -344,7 +362,9 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
             // V tile (w = 2; the tile's two halves back to back)
             {
                 const int b = lane / 3, w = lane - 3 * b;
-                const int pid = __shfl_sync(0xffffffffu, id, b & 31);
+                const int j = (b0 + b) & 63;  // in range whenever b < nb
+                const int lo = __shfl_sync(0xffffffffu, ids[0], j & 31), hi = __shfl_sync(0xffffffffu, ids[1], j & 31);
+                const int pid = j < 32 ? lo : hi;
                 if (b < nb) {
                     const int y = (pid * p.num_kv_heads + kvh) * BS;  // row of the tile in [rows][128]
                     if (w < 2)
@@ -587,9 +607,11 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 
-    if (p.fuse_merge) {
+    if (p.fuse_merge && flags[3]) {
         // One arrival per (member, head tile of the decode kernel) that takes
         // a partial from this partition; the last arrival merges the row.
+        // (Members with partitions of their own are merged by the decode
+        // kernel, which folds these partials in or counts them.)
         const int units = nmem * p.head_tiles;
         __threadfence();
         __syncthreads();
