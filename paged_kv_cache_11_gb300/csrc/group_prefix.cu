@@ -36,7 +36,7 @@
 //
 // The partition streams through in chunks of 64 tokens, pipelined across
 // three roles that hand off on mbarriers:
-//   TMA warp: the chunk's (block, KV head) tiles of K and V into a 4-stage
+//   TMA warp: the chunk's (block, KV head) tiles of K and V into a 5-stage
 //     ring.  K lands as two [64 tokens][64 dims] halves, tokens contiguous
 //     across the chunk's blocks (one copy per block and half); V lands tile
 //     after tile, each as its two [BS][64] halves (one copy per tile).  The
@@ -46,10 +46,9 @@
 //     each product's completion is signalled by tcgen05.commit;
 //   softmax warps 0-3 (TMEM lanes 0-127): S(c) from TMEM, the online softmax
 //     in the log2 domain with the running max raised lazily (as in the decode
-//     warp core; O and l are rescaled when it is), P(c) into one of two
-//     shared-memory buffers, and at the end the normalised output and
-//     log-sum-exp.  A chunk's softmax waits for the previous chunk's product
-//     only when it has to rescale O.
+//     warp core; O and l are rescaled when it is), P(c) into shared memory
+//     once the previous chunk's product has read it, and at the end the
+//     normalised output and log-sum-exp.
 // Every wait is bounded; a wait that runs out records PKV_DEVERR_TIMEOUT,
 // the roles stop at the same chunk, and the copies and products already
 // issued are waited for before the CTA frees its tensor memory.
@@ -63,7 +62,8 @@ constexpr int kMmaWarp = kSoftWarps + 1;  // tensor-core products (lane 0)
 constexpr int kPrefixThreads = (kSoftWarps + 2) * 32;
 constexpr int kChunk = 64;                // tokens per pipeline step
 constexpr int kUmmaM = 128;               // M of both products
-constexpr int kRing = 4;                  // K/V chunks in flight
+constexpr int kRing = 5;                  // K/V chunks in flight
+constexpr int kPBufs = 1;                 // P buffers (a chunk's P waits for the product kPBufs chunks back)
 constexpr uint32_t kTmemCols = 256;       // S: [0, 64) and [64, 128); O: [128, 256)
 constexpr uint32_t kOCol = 128;
 
@@ -162,14 +162,14 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) { return r * 128 +
 struct PrefixSmem {
     static constexpr int kQHalf = kUmmaM * 128;   // Q: [128 rows][64 dims] per dims half, 16 KiB
     static constexpr int kKVHalf = kChunk * 128;  // a chunk of K or V: [64 tokens][64 dims] per dims half, 8 KiB
-    static constexpr int kPBuf = kUmmaM * 128;    // P: [128 rows][64 tokens], 16 KiB; two buffers
+    static constexpr int kPBuf = kUmmaM * 128;    // P: [128 rows][64 tokens], 16 KiB per buffer
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + 2 * kQHalf;
     static constexpr int kVOff = kKOff + kRing * 2 * kKVHalf;
     static constexpr int kPOff = kVOff + kRing * 2 * kKVHalf;
-    static constexpr int kBarOff = kPOff + 2 * kPBuf;
-    // kvfull[kRing], kvempty[kRing], sfull[2], sfree[2], pfull[2], pvdone[2]
-    static constexpr int kNumBars = 2 * kRing + 8;
+    static constexpr int kBarOff = kPOff + kPBufs * kPBuf;
+    // kvfull[kRing], kvempty[kRing], sfull[2], sfree[2], pfull[kPBufs], pvdone[kPBufs]
+    static constexpr int kNumBars = 2 * kRing + 4 + 2 * kPBufs;
     static constexpr int kSlotOff = kBarOff + kNumBars * 8;
     // per member of the tile: sequence, prefix tokens (0 when it takes no
     // part), partitions in all, whether the prefix side merges; per (member,
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     float* xch = reinterpret_cast<float*>(smem + S::kXchOff);
     const uint32_t bar0 = smem_addr(smem + S::kBarOff);
     const uint32_t kvfull0 = bar0, kvempty0 = bar0 + 8 * kRing, sfull0 = bar0 + 16 * kRing, sfree0 = sfull0 + 16,
-                   pfull0 = sfree0 + 16, pvdone0 = pfull0 + 16;
+                   pfull0 = sfree0 + 16, pvdone0 = pfull0 + 8 * kPBufs;
     const uint32_t slot = smem_addr(smem + S::kSlotOff);
     uint8_t* const qreg = smem + S::kQOff;
     uint8_t* const preg = smem + S::kPOff;
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
             mbar_init(sfull0 + 8 * i, 1);
             mbar_init(sfree0 + 8 * i, kSoftWarps);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kPBufs; ++i) {
             mbar_init(pfull0 + 8 * i, kSoftWarps);
             mbar_init(pvdone0 + 8 * i, 1);
         }
@@ -411,8 +411,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                 }
                 if (c < 0) continue;
                 // O += P(c) V(c): rows 0-63 the high part, rows 64-127 the residual
-                const int pb = c & 1;
-                ok = mbar_wait(pfull0 + 8 * pb, (c >> 1) & 1);
+                const int pb = c % kPBufs;
+                ok = mbar_wait(pfull0 + 8 * pb, (c / kPBufs) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 const int st = c % kRing;
@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                 umma_commit(kvempty0 + 8 * st);
                 umma_commit(pvdone0 + 8 * pb);
                 last_bar = pvdone0 + 8 * pb;
-                last_par = (c >> 1) & 1;
+                last_par = (c / kPBufs) & 1;
             }
             if (!ok) {
                 atomicOr(flags, 2);
@@ -448,7 +448,9 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         float l = 0.f;  // this half's share of the row sum
         bool ok = true;
         // Wait for the product of chunk j (warp-uniform verdict).
-        auto pv_done = [&](int j) { return __all_sync(0xffffffffu, mbar_wait(pvdone0 + 8 * (j & 1), (j >> 1) & 1)); };
+        auto pv_done = [&](int j) {
+            return __all_sync(0xffffffffu, mbar_wait(pvdone0 + 8 * (j % kPBufs), (j / kPBufs) & 1));
+        };
         for (int c = 0; c < nchunks; ++c) {
             const int sb = c & 1;
             float v[32];
@@ -496,12 +498,12 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                 lo[e] = pack2<kBF16>(p0 - r0, p1 - r1);
             }
             // O is rescaled once the previous chunk's product is in it; the P
-            // buffer is reused once the product two chunks back has read it
+            // buffer is reused once the product kPBufs chunks back has read it
             const bool rescale = c > 0 && __any_sync(0xffffffffu, alpha != 1.f);
             if (rescale)
                 ok = pv_done(c - 1);
-            else if (c >= 2)
-                ok = pv_done(c - 2);
+            else if (c >= kPBufs)
+                ok = pv_done(c - kPBufs);
             if (!ok) {
                 if (lane == 0) flags[2] = 1;  // the next softmax_sync stops every softmax warp
                 continue;
@@ -521,7 +523,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
             }
             // tokens 32 half .. +31 (16-byte chunks 4 half .. +3): the high
             // part into row r, the residual into row r + 64
-            uint8_t* pbuf = preg + sb * S::kPBuf;
+            uint8_t* pbuf = preg + (c % kPBufs) * S::kPBuf;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int cc = 4 * half + q;
@@ -533,7 +535,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
             fence_proxy_async_shared();  // the tensor cores read P through the async proxy
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(pfull0 + 8 * sb);
+            if (lane == 0) mbar_arrive(pfull0 + 8 * (c % kPBufs));
         }
         if (ok) ok = pv_done(nchunks - 1);
         tc_fence_after();
