@@ -74,6 +74,36 @@ def test_shared_prefix_step(gpu, bs):
     assert pkv.check_device_error() == 0
 
 
+@pytest.mark.parametrize("bs,dtype", [(16, "bf16"), (32, "fp16")])
+def test_prefix_running_max_raised(gpu, bs, dtype):
+    """Scores that jump far above the running max in later 64-token chunks of
+    the shared prefix: the prefix kernel raises its max and rescales the
+    output accumulator in tensor memory twice, then accumulates a score just
+    below the new max without a raise.  Every query is a multiple of one
+    direction u; the shared K rows at prefix tokens 40, 170, 300 and 460 are
+    multiples of u whose scores are about 16, 26, 36 and 37 in log2 units."""
+    members = [[(512, 600), (512, 530), (512, 512), (256, 700)]]
+    wl, gs, pl, mg = W.make_grouped_workload(21, members, 8, 2, bs, dtype)  # G = 4
+    D = 128
+    u = np.where(np.arange(D) % 3 == 0, 1.0, -1.0).astype(np.float32)
+    lead = 0  # the group's first member holds the shared blocks in its table
+    for t, c in ((40, 1.0), (170, 1.6), (300, 2.2), (460, 2.25)):
+        pb = int(wl.block_tables[lead][t // bs])
+        for kvh in range(wl.k_cache.shape[1]):
+            wl.k_cache[pb, kvh, t % bs] = W.round_f32(c * u, dtype)
+    wl.q[:] = W.round_f32(np.broadcast_to(u, wl.q.shape), dtype)
+    wl.poison()
+    kc, vc, out = run_grouped(wl, gs, pl, mg, gpu)
+    ref = oracle_out(wl)
+    assert max_abs_err(out, ref) <= TOL
+    # the decode kernel's warp core raises its max the same way (plain decode)
+    plain = pkv.paged_attention_decode(to_dev(wl.q, wl.dtype, gpu), kc, vc, _dev(wl.block_tables, gpu),
+                                       _dev(wl.context_lens, gpu), wl.scale, max_context_len=wl.max_context_len)
+    torch.cuda.synchronize()
+    assert max_abs_err(plain, ref) <= TOL
+    assert pkv.check_device_error() == 0
+
+
 @pytest.mark.parametrize("groups", [16, 32])
 def test_long_prefix_partitions(gpu, groups):
     """Enough groups for the call to take longer prefix partitions (on one
