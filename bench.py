@@ -112,12 +112,22 @@ def measured_peaks() -> dict:
     return {}
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments and blank lines (no string literal in
+    these sources holds a comment marker)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", line).rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def decode_source_hash() -> str:
-    """sha256[:16] over the sources the decode kernels are built from."""
+    """sha256[:16] over the code (comments dropped) of the sources the decode
+    kernels are built from."""
     import hashlib
     h = hashlib.sha256()
     for name in ("decode.cu", "group_prefix.cu", "decode_common.cuh", "pkv_internal.cuh"):
-        h.update((ROOT / "paged_kv_cache_11_gb300" / "csrc" / name).read_bytes())
+        h.update(_code_only((ROOT / "paged_kv_cache_11_gb300" / "csrc" / name).read_text()).encode())
     return h.hexdigest()[:16]
 
 

@@ -91,7 +91,7 @@ constexpr int kPrefixPartition = 256;
 constexpr int kPrefixPartitionMax = 1024;
 // Resident prefix CTAs per SM (about 197 KiB of shared memory each).
 constexpr int kPrefixCtasPerSm = 1;
-// Query rows of one prefix CTA (4 consumer warps x 16 rows).
+// Query rows of one prefix CTA (each fed twice to the prefix kernel's M = 128 products).
 constexpr int kPrefixRows = 64;
 
 // Query heads of one GQA group handled by one decode CTA (8 or 16).
