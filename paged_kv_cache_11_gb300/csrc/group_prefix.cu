@@ -154,6 +154,12 @@ __device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence
 // Barrier over the softmax warps only (named barrier 1).
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftWarps * 32) : "memory"); }
 
+// Barrier over the softmax warps and the MMA warp, not the TMA warp (named
+// barrier 2): Q is in shared memory and the TMEM columns are allocated.
+__device__ __forceinline__ void compute_sync() {
+    asm volatile("bar.sync 2, %0;" ::"n"((kSoftWarps + 1) * 32) : "memory");
+}
+
 // Byte offset of 16-byte chunk c (0-7) of row r in a [rows][64 x 16-bit]
 // region with the 128-byte swizzle (the layout TMA writes and the
 // descriptors above read).
@@ -283,7 +289,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     const int nchunks = (ntok + kChunk - 1) / kChunk;
     const int rows = nmem * G;  // <= 64
 
-    // ---- TMEM (MMA warp), Q rows into shared memory (softmax warps)
+    // ---- TMEM (MMA warp), Q rows into shared memory (softmax warps).  The
+    // TMA warp needs neither and starts its copies at once.
     if (warp == kMmaWarp) tmem_alloc(slot, kTmemCols);
     if (warp < kSoftWarps) {
         // Q rows of the tile (row r: member r / G, head r % G of its KV head),
@@ -310,10 +317,13 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         }
         fence_proxy_async_shared();  // the tensor cores read Q through the async proxy
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kSlotOff);
+    uint32_t tmem = 0;
+    if (warp != kTmaWarp) {
+        tc_fence_before();
+        compute_sync();
+        tc_fence_after();
+        tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kSlotOff);
+    }
 
     float m_run = -INFINITY;  // softmax threads: running max of the row (raised lazily)
 
