@@ -31,8 +31,9 @@
 // plus a 16-bit residual: row r of P's A operand is the high part of query
 // row r and row r + 64 its residual, so one product accumulates both, in
 // lanes r and r + 64 of O, which the epilogue adds.  (A tcgen05.mma with
-// M = 128 costs about the same for any N up to 128, so the rows a product
-// carries matter more than its width.)
+// M = 128 costs the tensor core about the same time for any N up to 64 and
+// about a third more at 128, so the rows a product carries matter more
+// than its width.)
 //
 // The partition streams through in chunks of 64 tokens, pipelined across
 // three roles that hand off on mbarriers:
@@ -49,9 +50,10 @@
 //     warp core; O and l are rescaled when it is), P(c) into shared memory
 //     once the previous chunk's product has read it, and at the end the
 //     normalised output and log-sum-exp.
-// Every wait is bounded; a wait that runs out records PKV_DEVERR_TIMEOUT,
-// the roles stop at the same chunk, and the copies and products already
-// issued are waited for before the CTA frees its tensor memory.
+// Every wait is bounded; a wait that runs out records PKV_DEVERR_TIMEOUT.
+// The softmax warps then stop together at the next chunk and the other roles
+// at their next wait; the copies and products already issued are waited for
+// (bounded) before the CTA frees its tensor memory or exits.
 #include "decode_common.cuh"
 
 namespace pkv {
