@@ -366,6 +366,17 @@ pkv_status compact_tokens(const int64_t* src_slots, const int64_t* dst_slots, in
  */
 pkv_status pkv_check_device_error(void* stream, int32_t* first_error_code);
 
+/*
+ * Self-test of the bounded-wait error path, with no fault and no hang.
+ * Launches one CTA that waits, through the same bounded mbarrier wait the
+ * copy pipelines use but with a limit of limit_us microseconds, on a phase
+ * that nothing completes.  The wait runs out, the CTA records
+ * PKV_DEVERR_TIMEOUT in the device error word (as a stalled pipeline would)
+ * and returns; the context stays usable.  limit_us: 1 .. 2,000,000, else
+ * PKV_ERR_INVALID_ARG with nothing launched.  Asynchronous on `stream`.
+ */
+pkv_status pkv_wait_selftest(int32_t limit_us, void* stream);
+
 /* Number of kernels this library has launched in this process. */
 uint64_t pkv_launch_count(void);
 

@@ -13,5 +13,6 @@ from .binding import (  # noqa: F401
     launch_count, paged_attention_append_decode, paged_attention_decode, paged_attention_decode_grouped,
     paged_attention_decode_static, paged_attention_grouped_workspace_bytes, paged_attention_partition_size,
     paged_attention_plan, paged_attention_workspace_bytes, paged_kv_append, status_string, swap_blocks, version,
+    wait_selftest,
 )
 from .block_manager import BlockManager, OutOfBlocks  # noqa: F401

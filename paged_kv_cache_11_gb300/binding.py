@@ -90,6 +90,8 @@ def _lib() -> ctypes.CDLL:
     lib.compact_tokens.restype = ctypes.c_int
     lib.pkv_check_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     lib.pkv_check_device_error.restype = ctypes.c_int
+    lib.pkv_wait_selftest.argtypes = [i32, vp]
+    lib.pkv_wait_selftest.restype = ctypes.c_int
     _LIB = lib
     return lib
 
@@ -347,6 +349,13 @@ def compact_tokens(src_slots: torch.Tensor, dst_slots: torch.Tensor, k_cache: to
     desc = cache_desc(k_cache)
     _check(_lib().compact_tokens(_ptr(src_slots), _ptr(dst_slots), src_slots.numel(), _ptr(k_cache), _ptr(v_cache),
                                  ctypes.byref(desc), _stream(stream)), "compact_tokens")
+
+
+def wait_selftest(limit_us: int = 50_000, stream=None) -> None:
+    """pkv_wait_selftest: one CTA's bounded wait on a phase nothing completes
+    runs out after limit_us and records PKV_DEVERR_TIMEOUT (read it with
+    check_device_error)."""
+    _check(_lib().pkv_wait_selftest(int(limit_us), _stream(stream)), "pkv_wait_selftest")
 
 
 def check_device_error(stream=None) -> int:

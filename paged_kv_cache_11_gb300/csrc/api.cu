@@ -198,6 +198,20 @@ static Plan make_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t head_tiles
 
 using namespace pkv;
 
+// pkv_wait_selftest: one thread waits on phase 0 of a fresh mbarrier that
+// expects one arrival nobody makes; the bounded wait runs out after limit_ns
+// and the error is recorded the way the copy pipelines record theirs.
+__global__ void wait_selftest_kernel(int* err, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    pdl_wait();
+    if (threadIdx.x == 0) {
+        const uint32_t b = smem_addr(&bar);
+        mbar_init(b, 1);
+        fence_barrier_init();
+        if (!mbar_wait_for(b, 0, limit_ns)) record_error(err, PKV_DEVERR_TIMEOUT);
+    }
+}
+
 extern "C" {
 
 const char* pkv_status_string(pkv_status s) {
@@ -577,6 +591,17 @@ pkv_status compact_tokens(const int64_t* src_slots, const int64_t* dst_slots, in
     const cudaError_t e = launch_compact(p, static_cast<cudaStream_t>(stream), &launches);
     g_launches += launches;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_wait_selftest(int32_t limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 2000000) return PKV_ERR_INVALID_ARG;
+    int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+    const cudaError_t e = launch_pdl(wait_selftest_kernel, dim3(1), dim3(32), 0, static_cast<cudaStream_t>(stream), err,
+                                     (uint64_t)limit_us * 1000ull);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    ++g_launches;
+    return PKV_OK;
 }
 
 pkv_status pkv_check_device_error(void* stream, int32_t* first_error_code) {

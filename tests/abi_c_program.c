@@ -16,7 +16,7 @@ int main(void) {
         (const void*)paged_attention_append_decode, (const void*)paged_attention_decode_grouped,
         (const void*)paged_attention_grouped_workspace_bytes, (const void*)paged_attention_decode_static,
         (const void*)copy_blocks, (const void*)swap_blocks, (const void*)compact_tokens,
-        (const void*)pkv_check_device_error, (const void*)pkv_launch_count};
+        (const void*)pkv_check_device_error, (const void*)pkv_launch_count, (const void*)pkv_wait_selftest};
     size_t i;
     pkv_cache_desc desc;
     for (i = 0; i < sizeof(entry) / sizeof(entry[0]); ++i)
@@ -33,6 +33,8 @@ int main(void) {
                                0.1f, (void*)16, PKV_FP32, &desc, 0, NULL, 0, NULL) != PKV_ERR_UNSUPPORTED)
         return 6;
     if (paged_kv_append(NULL, NULL, NULL, 0, NULL, NULL, NULL, NULL) != PKV_ERR_INVALID_ARG) return 7;
+    if (pkv_wait_selftest(0, NULL) != PKV_ERR_INVALID_ARG) return 8; /* limit out of range: nothing launched */
+    if (pkv_wait_selftest(2000001, NULL) != PKV_ERR_INVALID_ARG) return 9;
     printf("c abi ok, version %d\n", pkv_version());
     return 0;
 }
