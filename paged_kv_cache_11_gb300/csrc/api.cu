@@ -58,7 +58,9 @@ static EncodeTiledFn encode_fn() {
 // KV head) tile.  Rank 3: the same memory as [2 halves][rows][64], the two
 // halves of a row 128 bytes apart, box [2][BS][64]: one copy brings the
 // whole tile as its two halves back to back, the layout the rank-2 copies
-// of both halves give.  Every coordinate stays inside the pool.
+// of both halves give.  Every coordinate stays inside the pool.  No L2
+// promotion: every copy is a whole contiguous tile half or tile, and
+// promotion to 256-byte lines measured slightly slower on decode.
 static pkv_status encode_cache_map(CUtensorMap* m, const void* base, const pkv_cache_desc& c, int rank) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return PKV_ERR_CUDA;
@@ -72,13 +74,13 @@ static pkv_status encode_cache_map(CUtensorMap* m, const void* base, const pkv_c
         const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
         const cuuint32_t box[2] = {64, (cuuint32_t)c.block_size};
         r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
         const cuuint64_t dims[3] = {64, rows, 2};
         const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, 128};
         const cuuint32_t box[3] = {64, (cuuint32_t)c.block_size, 2};
         r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_INVALID_ARG;
 }
