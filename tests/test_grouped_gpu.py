@@ -74,6 +74,33 @@ def test_shared_prefix_step(gpu, bs):
     assert pkv.check_device_error() == 0
 
 
+@pytest.mark.slow
+def test_full_size_step_sampled(gpu):
+    """The shared-prefix step the benchmark times, at full size (16 groups x 16
+    members, 1024-token prompt, 256 sequences): copy-on-write, the 68k-token
+    append, then the grouped call with its automatic partitions.  The pools
+    are compared bit for bit; outputs are sampled against the oracle (every
+    group's first and last member, plus random rows)."""
+    wl = W.make_workload("shared_prefix")
+    dev, dt = gpu, wl.dtype
+    kc, vc = to_dev(wl.k_cache, dt, dev), to_dev(wl.v_cache, dt, dev)
+    pkv.copy_blocks(kc, vc, _dev(wl.cow_pairs, dev))
+    pkv.paged_kv_append(to_dev(wl.new_k, dt, dev), to_dev(wl.new_v, dt, dev), _dev(wl.slot_mapping, dev), kc, vc)
+    gs, pl, mg = W.prefix_groups(wl)
+    assert len(gs) - 1 == 16 and mg == 16 and (pl >= 1024).all()
+    _, _, out = run_grouped(wl, gs, pl, mg, dev, kc=kc, vc=vc)
+    rng = np.random.default_rng(5)
+    sel = {(int(s), int(h)) for s, h in zip(rng.integers(0, wl.num_seqs, 64), rng.integers(0, wl.num_q_heads, 64))}
+    for g in range(len(gs) - 1):
+        sel |= {(int(gs[g]), 0), (int(gs[g + 1]) - 1, wl.num_q_heads - 1)}
+    sel = sorted(sel)
+    okc, ovc, ref = oracle_step(wl, select=sel, in_place=True)
+    assert np.array_equal(to_bits(kc), okc) and np.array_equal(to_bits(vc), ovc)
+    assert max_abs_err(out, ref, select=sel) <= TOL
+    assert torch.isfinite(out).all()
+    assert pkv.check_device_error() == 0
+
+
 @pytest.mark.parametrize("bs,dtype", [(16, "bf16"), (32, "fp16")])
 def test_prefix_running_max_raised(gpu, bs, dtype):
     """Scores that jump far above the running max in later 64-token chunks of
