@@ -1,0 +1,33 @@
+"""Host-side pieces of bench.py that decide what its JSON line reports (no GPU)."""
+from pathlib import Path
+
+import bench
+
+CSRC = Path(bench.__file__).resolve().parent / "paged_kv_cache_11_gb300" / "csrc"
+
+
+def test_code_only_drops_comments_and_blank_lines():
+    src = "int a; // trailing\n\n/* block\n comment */int b;\n  // whole line\nint c;  \n"
+    assert bench._code_only(src) == "int a;\nint b;\nint c;"
+
+
+def test_comment_edits_keep_the_code_hash_and_code_edits_change_it():
+    text = (CSRC / "decode.cu").read_text()
+    base = bench._code_only(text)
+    assert bench._code_only(text.replace("// Grid:", "// The grid:", 1)) == base
+    assert bench._code_only(text + "\n/* a note */\n") == base
+    assert bench._code_only(text.replace("const int tid = threadIdx.x", "const int tid = (int)threadIdx.x", 1)) != base
+
+
+def test_traffic_figure_is_reported_only_for_the_code_it_was_taken_on():
+    """A traffic entry is used when its key is the current decode code's hash,
+    and ignored (the bench line reports null) otherwise."""
+    h = bench.decode_source_hash()
+    lines = [l.split() for l in bench.TRAFFIC_FILE.read_text().splitlines() if l and not l.startswith("#")]
+    assert lines and all(len(l) == 3 for l in lines)
+    for workload, key, value in lines:
+        got = bench.traffic_per_launch(workload)
+        assert (got is not None) == (key == h), (workload, key, h)
+        if got is not None:
+            assert got == float(value)
+    assert bench.traffic_per_launch("no_such_workload") is None
