@@ -40,6 +40,7 @@ METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak); sequences/s per 
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = ROOT / "profiles" / "traffic_per_launch.txt"
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 
 
 def parse_args(argv=None):
@@ -584,6 +585,7 @@ def run_ours(args):
                        wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, mcl, args.partition_size)},
         "seq_per_s": seqs_all * steps / (ms_max / 1e3),
         "pct_of_hbm_peak": 100.0 * value / peak,
+        "pct_of_nominal_hbm": 100.0 * value / NOMINAL_HBM_GBS,  # the part's nominal 8 TB/s, for context
         "roofline": {"kernel": dec_api + (" (shared-prefix kernel + decode kernel + merge; bytes: each distinct "
                                           "K/V slot once)" if grouped else " (decode kernel + split-K merge)"),
                      "bound": "hbm",
