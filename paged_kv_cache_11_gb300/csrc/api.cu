@@ -146,7 +146,7 @@ static int sm_count() {
 }
 
 // Tokens per split-K partition.  An explicit size is used as given.  The
-// automatic choice takes the largest of 512, 1024, 2048 tokens for which the
+// automatic choice takes the largest of 512, 1024, 2048, 4096 tokens for which the
 // work units (sequence x KV head x head tile x partition, counted at
 // max_context_len) still fill the GPU's resident decode CTAs at least twice;
 // longer partitions amortise each CTA's start-up, shorter ones balance the
@@ -155,7 +155,7 @@ static int resolve_partition(int32_t partition_size, int64_t rows, int32_t max_c
     if (partition_size != 0) return partition_size;
     const int64_t slots = (int64_t)(sm_count() > 0 ? sm_count() : 148) * kDecodeCtasPerSm;
     int best = kAutoPartition;
-    for (int P = 1024; P <= 2048; P *= 2) {
+    for (int P = 1024; P <= 4096; P *= 2) {
         const int64_t units = rows * (((int64_t)max_context_len + P - 1) / P);
         if (units >= 2 * slots) best = P;
     }

@@ -104,7 +104,7 @@ def test_plan_query(lib):
 def test_partition_size_query(lib):
     assert binding.paged_attention_partition_size(8, 64, 8, 131072, 256) == 256   # explicit: as given
     assert binding.paged_attention_partition_size(8, 64, 7, 131072, 0) == 0       # 64 % 7 != 0
-    assert binding.paged_attention_partition_size(8, 64, 8, 131072, 0) in (512, 1024, 2048)
+    assert binding.paged_attention_partition_size(8, 64, 8, 131072, 0) in (512, 1024, 2048, 4096)
 
 
 def test_workspace_bytes(lib):
