@@ -107,6 +107,17 @@ def test_partition_size_query(lib):
     assert binding.paged_attention_partition_size(8, 64, 8, 131072, 0) in (512, 1024, 2048, 4096)
 
 
+def test_partition_choice_for_the_benchmark_shapes(lib):
+    """The automatic split-K partition: the largest of 512..4096 tokens that still
+    gives two waves of work units.  Without a GPU the library assumes 148 SMs;
+    these choices are the same with the GB300's 152."""
+    f = binding.paged_attention_partition_size
+    assert f(64, 32, 8, 4096, 0) == 1024      # llama8b: 512 rows x 4 partitions
+    assert f(8, 64, 8, 131072, 0) == 4096     # llama70b_long: 64 rows x 32 partitions
+    assert f(128, 40, 40, 2048, 0) == 4096    # opt13b: one partition per row either way
+    assert f(4, 4, 1, 100, 0) == 512          # too little work for longer partitions
+
+
 def test_workspace_bytes(lib):
     assert binding.paged_attention_workspace_bytes(8, 64, 128, 512, 0) == 0          # one partition
     n = binding.paged_attention_workspace_bytes(8, 64, 128, 131072, 0)
