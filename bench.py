@@ -3,15 +3,22 @@
 
 One step = copy_blocks of the workload's copy-on-write pairs (when it has
 any) + paged_kv_append of the step's new tokens + paged_attention_decode over
-every sequence.  The default workload is the Llama-3-8B-class layer (64
-sequences, 32 query / 8 KV heads, bf16, block 16, contexts uniform in
-[512, 4096]); ``--workload`` selects another one.
+every sequence; a step that appends one token per sequence at its last
+position is the single fused call paged_attention_append_decode.
+
+The default workload is the Llama-3.1-70B-class long-context layer (8
+sequences of 131072 tokens, 64 query / 8 KV heads, bf16, block 32: 4 GiB of
+K/V per step), the largest configuration on one GPU; the Llama-3-8B-class
+layer (64 sequences, 32 query / 8 KV heads, bf16, block 16, contexts uniform
+in [512, 4096]) is measured after it in the same run and reported under
+``per_workload``.  ``--workload`` selects another main workload and
+``--extra`` the others.
 
 Metric: K/V bytes of the attended contexts per second (GB/s) and sequences per
 second; the roofline object reports paged_attention_decode's algorithmic
 bytes per launch over its CUDA-event time against the measured HBM peak.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME] [--extra A,B]
 
 Under torchrun (N > 1) every rank runs its own batch (different seed) with no
 data exchange; timing is the max over ranks and value aggregates all ranks.
@@ -49,7 +56,10 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--workload", default="llama70b_long")
+    ap.add_argument("--extra", default=None,
+                    help="comma-separated workloads measured after the main one and reported under per_workload "
+                         "(default: llama8b when the main workload is llama70b_long, else none)")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seqs", type=int, default=0, help="0: the whole batch")
@@ -146,7 +156,9 @@ def traffic_per_launch(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms; the
+    summary covers the samples taken inside the marked intervals (each
+    workload's warm-up, timed region and per-step statistics run)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -155,7 +167,7 @@ class ClockSampler:
         self.dev = device_index
         self.samples = []
         self.proc = None
-        self.t0 = self.t1 = None
+        self.spans = []
 
     def start(self):
         try:
@@ -174,21 +186,12 @@ class ClockSampler:
 
     def mark(self, begin: bool):
         if begin:
-            self.t0 = time.time()
-        else:
-            self.t1 = time.time()
+            self.spans.append([time.time(), None])
+        elif self.spans:
+            self.spans[-1][1] = time.time()
 
-    def stop(self) -> dict | None:
-        if self.proc is None:
-            return None
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        lo, hi = (self.t0 or 0) - 0.15, (self.t1 or time.time()) + 0.15
-        rows = [s for t, s in self.samples if lo <= t <= hi] or [s for _, s in self.samples[-3:]]
+    @staticmethod
+    def summarise(rows) -> dict | None:
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -207,6 +210,21 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        spans = [(a, b if b is not None else time.time()) for a, b in self.spans]
+        rows = [s for t, s in self.samples if any(a <= t <= b for a, b in spans)]
+        if not rows:  # intervals shorter than the sampling period: the nearest samples
+            rows = [s for t, s in self.samples if any(a - 0.15 <= t <= b + 0.15 for a, b in spans)]
+        return self.summarise(rows)
 
 
 # ---------------------------------------------------------------- workload description
@@ -247,7 +265,7 @@ def decode_algorithmic_bytes(wl, fused: bool = False, groups=None) -> int:
 # ---------------------------------------------------------------- CPU oracle timing
 def time_oracle(wl, nseq: int, threads: int):
     """One oracle step (copy + append + decode) over the first nseq sequences; returns
-    (seconds, kv_bytes, sequences)."""
+    (seconds, kv_bytes, sequences, outputs [B, Hq, D] float64 with those sequences filled)."""
     import oracle
     nseq = min(nseq or wl.num_seqs, wl.num_seqs)
     sel = [(s, h) for s in range(nseq) for h in range(wl.num_q_heads)]
@@ -258,10 +276,11 @@ def time_oracle(wl, nseq: int, threads: int):
     if len(wl.slot_mapping):
         m = wl.append_seq < nseq
         oracle.append(np.ascontiguousarray(wl.new_k[m]), np.ascontiguousarray(wl.new_v[m]), wl.slot_mapping[m], kc, vc)
-    oracle.decode(wl.q, kc, vc, wl.block_tables, wl.context_lens, wl.scale, wl.dtype, select=sel, threads=threads)
+    out, _ = oracle.decode(wl.q, kc, vc, wl.block_tables, wl.context_lens, wl.scale, wl.dtype, select=sel,
+                           threads=threads)
     dt = time.perf_counter() - t0
     kvb = int(wl.context_lens[:nseq].astype(np.int64).sum()) * 2 * wl.num_kv_heads * wl.head_dim * 2
-    return dt, kvb, nseq
+    return dt, kvb, nseq, out
 
 
 def host_threads() -> int:
@@ -285,14 +304,14 @@ def run_reference(args):
     nseq = args.cpu_sample_seqs
     if not nseq:
         # size each step's sample so that warmup + steps take about a minute
-        t1, _, _ = time_oracle(wl, 1, threads)
+        t1 = time_oracle(wl, 1, threads)[0]
         per_step = 60.0 / max(1, args.steps + args.warmup)
         nseq = int(max(1, min(wl.num_seqs, 8, per_step // max(t1, 1e-6))))
     for _ in range(max(0, args.warmup)):
         time_oracle(wl, nseq, threads)
     tot, kvb, seqs = 0.0, 0, 0
     for _ in range(args.steps):
-        dt, b, n = time_oracle(wl, nseq, threads)
+        dt, b, n, _ = time_oracle(wl, nseq, threads)
         tot += dt
         kvb += b
         seqs += n
@@ -311,23 +330,36 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args):
-    import torch
+WARM_GPU_S = 0.5      # GPU time of warm-up steps run right before each timed region
+STAT_MIN_STEPS = 50   # per-step timings behind the median / p10 / p90
 
-    import paged_kv_cache_11_gb300 as pkv
-    from paged_kv_cache_11_gb300 import _build, workload as W
 
-    ws, rank, local = dist_env()
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist = init_dist(ws, "nccl")
-    _build.build_all()
-    pkv.binding._lib()
+def percentiles(xs) -> dict:
+    a = np.sort(np.asarray(xs, dtype=np.float64))
+    return {"median_ms": float(np.median(a)), "p10_ms": float(np.percentile(a, 10)),
+            "p90_ms": float(np.percentile(a, 90)), "n": int(len(a))}
 
-    spec = W.SPECS[args.workload]
-    wl = W.make_workload(args.workload, seed=rank_seed(W.default_seed(spec), rank))
+
+class Device:
+    """What every workload's measurement shares: the device, the stream, the
+    process group and the clock sampler."""
+
+    def __init__(self, torch, pkv, dev, rank, ws, dist, clocks):
+        self.torch, self.pkv, self.dev, self.rank, self.ws, self.dist, self.clocks = \
+            torch, pkv, dev, rank, ws, dist, clocks
+        self.stream = torch.cuda.current_stream()
+
+
+def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool) -> dict:
+    """One workload: warm-up, exactly args.steps timed steps, per-step
+    statistics, the end-to-end run through host buffers, and (rank 0 of a
+    one-process run) the oracle on the host cores over the same inputs, whose
+    outputs also give the maximum error of the GPU result."""
+    torch, pkv, dev, stream, dist = d.torch, d.pkv, d.dev, d.stream, d.dist
+    from paged_kv_cache_11_gb300 import workload as W
+
+    spec = W.SPECS[name]
+    wl = W.make_workload(name, seed=rank_seed(W.default_seed(spec), d.rank))
     dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[wl.dtype]
 
     def up(bits):
@@ -341,14 +373,14 @@ def run_ours(args):
     cow = torch.from_numpy(wl.cow_pairs).to(dev) if len(wl.cow_pairs) else None
     out = torch.empty((wl.num_seqs, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
     mcl = wl.max_context_len
-    stream = torch.cuda.current_stream()
 
     # A decode step that appends one token per sequence, at its last position,
-    # runs as one fused launch (block write + attention); other steps (the
-    # shared-prefix continuation) run copy_blocks, paged_kv_append, decode --
-    # the grouped decode when the batch holds forked groups.
+    # runs as one fused launch (block write + attention); other steps (with
+    # copy-on-write copies) run copy_blocks, paged_kv_append, decode -- the
+    # grouped decode when the batch holds forked groups.
     fused = (not args.unfused) and cow is None and np.array_equal(wl.append_seq, np.arange(wl.num_seqs))
     grouped = bool(spec.groups) and not args.ungrouped and not fused
+    g_starts = g_plen = gs_d = pl_d = None
     if grouped:
         g_starts, g_plen, g_max = W.prefix_groups(wl)
         g_mpl = int(g_plen.max())
@@ -370,9 +402,10 @@ def run_ours(args):
                                        partition_size=args.partition_size, workspace=ws_)
 
     def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+        """One step; ev = (start, end) events bracket its decode call."""
         if fused:
+            if ev is not None:
+                ev[0].record(stream)
             pkv.paged_attention_append_decode(q, nk, nv, sm, kc, vc, bt, cl, wl.scale, out=out, max_context_len=mcl,
                                               partition_size=args.partition_size, workspace=wsp)
         else:
@@ -382,36 +415,49 @@ def run_ours(args):
                 pkv.paged_kv_append(nk, nv, sm, kc, vc)
             if ev is not None:
                 ev[0].record(stream)
-            decode(q, bt, cl, out, wsp, gs_d if grouped else None, pl_d if grouped else None)
+            decode(q, bt, cl, out, wsp, gs_d, pl_d)
         if ev is not None:
             ev[1].record(stream)
 
+    def event_pair():
+        return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    if d.clocks:
+        d.clocks.mark(True)
+    # ---- warm-up: the requested steps, then more until WARM_GPU_S of GPU
+    # time has run, so that the clocks and the memory system are at their
+    # working state when the timed region starts (the GPU is never left idle
+    # in between; the only gap is the barrier and synchronisation).
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
-    assert pkv.check_device_error() == 0
+    assert pkv.check_device_error() == 0, "device error during warm-up"
+    warm_ms, batch = 0.0, 8
+    while warm_ms < 1e3 * WARM_GPU_S:
+        a, b = event_pair()
+        a.record(stream)
+        for _ in range(batch):
+            step()
+        b.record(stream)
+        b.synchronize()
+        ms = a.elapsed_time(b)
+        warm_ms += ms
+        batch = int(min(4096, max(batch, batch * 1e3 * WARM_GPU_S / max(ms, 1e-3) / 4)))
 
-    clocks = ClockSampler(local) if rank == 0 else None
-    if clocks:
-        clocks.start()
-        time.sleep(0.3)
-    # A step that is one launch (the fused decode) runs back to back between
-    # two events, so consecutive launches overlap as they do in a serving
-    # loop, and that launch's duration is the step's.  A step of several
-    # launches also brackets its decode call with events.
-    evs = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-           if not fused or args.flush_l2 else [None] * args.steps)
+    # ---- the timed region: exactly args.steps steps.  A step that is one
+    # launch (the fused decode) runs back to back between two events, so
+    # consecutive launches overlap as they do in a serving loop and that
+    # launch's duration is the step's.  A step of several launches also
+    # brackets its decode call with events.
+    evs = [event_pair() for _ in range(args.steps)] if (not fused or args.flush_l2) else [None] * args.steps
     # --flush-l2: each step is bracketed by its own events and the flush runs
     # between steps, outside them
-    step_evs = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(args.steps)] if args.flush_l2 else None)
+    step_evs = [event_pair() for _ in range(args.steps)] if args.flush_l2 else None
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start, t_end = event_pair()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    if clocks:
-        clocks.mark(True)
     l0 = pkv.launch_count()
     t_start.record(stream)
     for i in range(args.steps):
@@ -424,8 +470,6 @@ def run_ours(args):
     t_end.record(stream)
     torch.cuda.synchronize()
     launches = pkv.launch_count() - l0
-    if clocks:
-        clocks.mark(False)
     if dist:
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
@@ -434,8 +478,29 @@ def run_ours(args):
     if fused and step_evs is None:
         dec_avg_ms = ms_total / args.steps
     else:
-        dec_ms = [a.elapsed_time(b) for a, b in evs]
-        dec_avg_ms = sum(dec_ms) / len(dec_ms)
+        dec_avg_ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    assert pkv.check_device_error() == 0, "device error in the timed region"
+
+    # ---- per-step statistics: every step of a separate run of
+    # max(STAT_MIN_STEPS, steps) steps bracketed by its own events (which also
+    # bracket the decode call of a multi-launch step).  An event between two
+    # launches keeps the next one from starting while the previous one
+    # drains, so these times run slightly above the timed region's mean.
+    n_stat = max(STAT_MIN_STEPS, args.steps)
+    st_evs = [event_pair() for _ in range(n_stat)]
+    dec_evs = [event_pair() for _ in range(n_stat)] if not fused else None
+    for i in range(n_stat):
+        st_evs[i][0].record(stream)
+        step(dec_evs[i] if dec_evs else None)
+        st_evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    if d.clocks:
+        d.clocks.mark(False)
+    stats = percentiles([a.elapsed_time(b) for a, b in st_evs])
+    stats["how"] = ("each of %d steps bracketed by its own CUDA events on the launching stream (run after the "
+                    "timed region; the events keep consecutive launches from overlapping)" % n_stat)
+    if dec_evs:
+        stats["decode_call"] = percentiles([a.elapsed_time(b) for a, b in dec_evs])
     assert pkv.check_device_error() == 0
 
     # ---- end to end: host buffers in, result out, through the public API.
@@ -452,13 +517,14 @@ def run_ours(args):
     if grouped:
         host_parts += [("gs", g_starts, torch.int32), ("pl", g_plen, torch.int32)]
     offs, off = {}, 0
-    for name, arr, _ in host_parts:
-        offs[name] = off
+    for pname, arr, _ in host_parts:
+        offs[pname] = off
         off += (arr.nbytes + 255) // 256 * 256
     h2d = off
     h_in = torch.empty(h2d, dtype=torch.uint8).pin_memory()
-    for name, arr, _ in host_parts:
-        h_in[offs[name]:offs[name] + arr.nbytes].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).ravel()))
+    for pname, arr, _ in host_parts:
+        h_in[offs[pname]:offs[pname] + arr.nbytes].copy_(
+            torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).ravel()))
     d_in = [torch.empty(h2d, dtype=torch.uint8, device=dev) for _ in range(2)]
     d_out = [torch.empty_like(out) for _ in range(2)]
     h_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
@@ -466,8 +532,8 @@ def run_ours(args):
 
     def views(buf):
         v = {}
-        for name, arr, tdt in host_parts:
-            v[name] = buf[offs[name]:offs[name] + arr.nbytes].view(tdt).view(arr.shape)
+        for pname, arr, tdt in host_parts:
+            v[pname] = buf[offs[pname]:offs[pname] + arr.nbytes].view(tdt).view(arr.shape)
         return v
 
     dviews = [views(b) for b in d_in]
@@ -520,7 +586,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0, e1 = event_pair()
     torch.cuda.synchronize()
     e0.record(xs)
     e2e_run(e2e_steps)
@@ -530,7 +596,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     assert pkv.check_device_error() == 0
-    assert torch.equal(h_out[(e2e_steps - 1) % 2], out.cpu()), "end-to-end output differs from the resident run"
+    out_host = out.cpu()
+    assert torch.equal(h_out[(e2e_steps - 1) % 2], out_host), "end-to-end output differs from the resident run"
 
     # ---- aggregate over ranks
     kvb = float(wl.kv_bytes())
@@ -539,11 +606,6 @@ def run_ours(args):
     kv_all = sum_over_ranks(dist, kvb, dev)
     seqs_all = sum_over_ranks(dist, float(wl.num_seqs), dev)
     launches_all = int(sum_over_ranks(dist, float(launches), dev))
-    clk = clocks.stop() if clocks else None
-    if rank != 0:
-        if dist:
-            dist.destroy_process_group()
-        return 0
 
     peaks = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
@@ -552,54 +614,108 @@ def run_ours(args):
     value = kv_all * steps / (ms_max / 1e3) / 1e9
     dec_bytes = decode_algorithmic_bytes(wl, fused, (g_starts, g_plen) if grouped else None)
     achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
-    traffic = traffic_per_launch(args.workload + ("_grouped" if grouped else ""))
+    traffic = traffic_per_launch(name + ("_grouped" if grouped else ""))
     dec_api = ("paged_attention_append_decode" if fused else
                "paged_attention_decode_grouped" if grouped else "paged_attention_decode")
 
+    # ---- the oracle on the host cores (rank 0 of a one-process run): the
+    # CPU baseline, and the maximum error of the GPU output against it
     cpu = None
-    if ws == 1 and not args.no_cpu_baseline:
+    if d.ws == 1 and not args.no_cpu_baseline:
         threads = host_threads()
         t = b = reps = 0
-        while reps == 0 or t < 10.0:  # repeat whole oracle steps for about 10 s of CPU time
-            dt1, b1, n = time_oracle(wl, args.cpu_sample_seqs, threads)
+        ref = None
+        while reps == 0 or t < cpu_seconds:  # whole oracle steps, about cpu_seconds of CPU time
+            dt1, b1, n, ref = time_oracle(wl, args.cpu_sample_seqs, threads)
             t, b, reps = t + dt1, b + b1, reps + 1
+        gpu_out = out_host.numpy().astype(np.float64)[:n]
+        err = float(np.abs(gpu_out - ref[:n]).max())
         cpu = {"value": b / t / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{reps} oracle step(s) over the first {n} of {wl.num_seqs} sequences (all query "
-                         f"heads), {t:.1f} s on {threads} host threads"}
-        # the same oracle on one thread, over fewer sequences (about 3 s)
-        n1 = max(1, int(n * min(1.0, 3.0 / max(threads * t / reps, 1e-9))))
-        dt1, b1, n1 = time_oracle(wl, n1, 1)
-        cpu["single_thread"] = {"value": b1 / dt1 / 1e9, "unit": UNIT, "cores": 1,
-                                "sample": f"one oracle step over the first {n1} of {wl.num_seqs} sequences, "
-                                          f"{dt1:.1f} s on 1 host thread"}
+                         f"heads), {t:.1f} s on {threads} host threads",
+               "max_abs_err": err, "max_abs_err_over": f"{n * wl.num_q_heads * wl.head_dim} outputs "
+                                                       f"({n} sequences x {wl.num_q_heads} heads x {wl.head_dim})"}
+        if single_thread:
+            # the same oracle on one thread, over fewer sequences (about 3 s)
+            n1 = max(1, int(n * min(1.0, 3.0 / max(threads * t / reps, 1e-9))))
+            dt1, b1, n1, _ = time_oracle(wl, n1, 1)
+            cpu["single_thread"] = {"value": b1 / dt1 / 1e9, "unit": UNIT, "cores": 1,
+                                    "sample": f"one oracle step over the first {n1} of {wl.num_seqs} sequences, "
+                                              f"{dt1:.1f} s on 1 host thread"}
 
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps, "warmup": args.warmup,
-        "ms_per_step": ms_max / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": wl.dtype, "data": "synthetic",
-        "config": {**describe(wl), "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": ("256 MB written before every step, outside the step's timing" if args.flush_l2 else
-                          f"inputs larger than L2 ({wl.kv_bytes() / 1e6:.0f} MB of K/V vs 129 MB), no flush"),
-                   "api": dec_api if fused else "copy_blocks + paged_kv_append + " + dec_api,
-                   "partition_size": pkv.paged_attention_partition_size(
-                       wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, mcl, args.partition_size)},
-        "seq_per_s": seqs_all * steps / (ms_max / 1e3),
+    res = {
+        "value": value, "ms_per_step": ms_max / steps, "seq_per_s": seqs_all * steps / (ms_max / 1e3),
         "pct_of_hbm_peak": 100.0 * value / peak,
         "pct_of_nominal_hbm": 100.0 * value / NOMINAL_HBM_GBS,  # the part's nominal 8 TB/s, for context
+        "config": {**describe(wl), "parallelism": f"replicas x{d.ws}" if d.ws > 1 else "single GPU",
+                   "l2": ("256 MB written before every step, outside the step's timing" if args.flush_l2 else
+                          f"no flush ({wl.kv_bytes() / 1e6:.0f} MB of K/V per step vs 129 MB of L2)"),
+                   "api": dec_api if fused else "copy_blocks + paged_kv_append + " + dec_api,
+                   "partition_size": pkv.paged_attention_partition_size(
+                       wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, mcl, args.partition_size),
+                   "warmup_gpu_ms": warm_ms},
         "roofline": {"kernel": dec_api + (" (shared-prefix kernel + decode kernel + merge; bytes: each distinct "
                                           "K/V slot once)" if grouped else " (decode kernel + split-K merge)"),
                      "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src, "traffic": traffic,
                      "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_avg_ms},
+        "stats": stats,
+        "max_abs_err": cpu["max_abs_err"] if cpu else None,
         "e2e": {"value": kv_all * e2e_steps / (e2e_max / 1e3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "how": "one packed pinned-host->device copy of the step's inputs and one device->pinned-host copy "
                        "of its output per step, double-buffered on a copy stream; the K/V pool stays resident"},
         "gpu_launches": launches_all,
-        "clocks": clk,
         "cpu_baseline": cpu,
+        "dtype": wl.dtype,
     }
+    del kc, vc, wsp, wsp2, d_in, d_out
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args):
+    import torch
+
+    import paged_kv_cache_11_gb300 as pkv
+    from paged_kv_cache_11_gb300 import _build
+
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(ws, "nccl")
+    _build.build_all()
+    pkv.binding._lib()
+
+    extra = ([w for w in args.extra.split(",") if w] if args.extra is not None else
+             (["llama8b"] if args.workload == "llama70b_long" else []))
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    d = Device(torch, pkv, dev, rank, ws, dist, clocks)
+    main = measure(args.workload, args, d, cpu_seconds=10.0, single_thread=True)
+    others = {w: measure(w, args, d, cpu_seconds=3.0, single_thread=False) for w in extra if w != args.workload}
+    clk = clocks.stop() if clocks else None
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    line = {
+        "metric": METRIC, "value": main["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": main["dtype"], "data": "synthetic",
+        "config": main["config"], "seq_per_s": main["seq_per_s"],
+        "pct_of_hbm_peak": main["pct_of_hbm_peak"], "pct_of_nominal_hbm": main["pct_of_nominal_hbm"],
+        "roofline": main["roofline"], "stats": main["stats"], "max_abs_err": main["max_abs_err"],
+        "e2e": main["e2e"], "gpu_launches": main["gpu_launches"], "clocks": clk,
+        "cpu_baseline": main["cpu_baseline"],
+    }
+    if others:
+        line["per_workload"] = {w: {k: v for k, v in r.items() if k != "dtype"} for w, r in others.items()}
     print(json.dumps(line))
     if dist:
         dist.destroy_process_group()

@@ -31,3 +31,19 @@ def test_traffic_figure_is_reported_only_for_the_code_it_was_taken_on():
         if got is not None:
             assert got == float(value)
     assert bench.traffic_per_launch("no_such_workload") is None
+
+
+def test_percentiles_and_clock_summary():
+    p = bench.percentiles([1.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0, 8.0, 9.0, 10.0, 11.0])
+    assert p["median_ms"] == 6.0 and p["n"] == 11 and p["p10_ms"] == 2.0 and p["p90_ms"] == 10.0
+    rows = ["0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+            "garbage"]
+    c = bench.ClockSampler.summarise(rows)
+    assert c == {"sm_mhz": 2025.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 2}
+    assert bench.ClockSampler.summarise(["garbage"]) is None
+
+
+def test_default_run_measures_the_long_context_layer_and_the_8b_layer():
+    a = bench.parse_args([])
+    assert a.workload == "llama70b_long" and a.extra is None
