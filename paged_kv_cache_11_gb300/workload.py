@@ -20,9 +20,17 @@ The five workloads mirror the shapes the pages size (page, section):
 * ``shared_prefix`` -- parallel sampling (tonho.wtf "vllm", "como funciona"):
   16 groups of 16 sequences; each group's prompt of 1024 + t_g tokens
   (t_g uniform in [1, 15]) is mapped by all 16 samples (reference count 16),
-  so its last block is shared and partly filled; each sample then writes its
-  own 32-512 token continuation, the first write into the shared block
-  copying it (15 copies per group; the 16th sample writes in place).
+  so its last block is shared and partly filled; each sample holds its own
+  32-512 token continuation, whose first write into the shared block copied
+  it (15 copies per group; the 16th sample wrote in place).  The step is a
+  decode step: the 240 copy-on-write pairs of the shared partial blocks,
+  then one new token per sample (256 tokens), then attention.  The copies
+  are repeated every step; each rewrites the same bytes (the prompt's
+  partial block, whose slots past the prompt are then the first
+  continuation tokens of the copying samples).
+* ``shared_prefix_prefill`` -- the same batch, with each sample's whole
+  continuation written by the step (about 68k tokens appended) before the
+  attention.
 * ``llama70b_long`` -- Llama-3.1-70B-class long context (aitalk.it
   "PagedAttention e RadixAttention", opening: 0.31 MB per token, 128k tokens
   ~ 40 GB): 64 query / 8 KV heads, bf16, block 32, 8 sequences of 131072
@@ -140,6 +148,9 @@ class Spec:
     prefix: int = 0
     tail: tuple = (1, 15)
     suffix: tuple = (32, 512)
+    # "decode": the step appends each sample's last token; "continuation": its
+    # whole continuation
+    step: str = "decode"
 
     @property
     def kind(self) -> str:
@@ -151,6 +162,8 @@ SPECS = {
     "llama8b": Spec("llama8b", 1, 32, 8, 16, "bf16", num_seqs=64, lens=("uniform", 512, 4096)),
     "opt13b": Spec("opt13b", 2, 40, 40, 16, "fp16", num_seqs=128, lens=("uniform", 1, 2048)),
     "shared_prefix": Spec("shared_prefix", 3, 32, 8, 16, "bf16", groups=16, per_group=16, prefix=1024),
+    "shared_prefix_prefill": Spec("shared_prefix_prefill", 3, 32, 8, 16, "bf16", groups=16, per_group=16,
+                                  prefix=1024, step="continuation"),
     "llama70b_long": Spec("llama70b_long", 4, 64, 8, 32, "bf16", num_seqs=8, lens=("fixed", (131072,) * 8),
                           pool_factor=1.0),
 }
@@ -306,10 +319,19 @@ def make_workload(name: str, seed: int | None = None, with_data: bool = True, th
                 for i in range(M):
                     bm.fork(parent + g, g * M + i)
                 bm.free(parent + g)                          # the samples hold the prompt blocks
+            whole = spec.step == "continuation"
             for g in range(G):
                 for i in range(M):
                     s = g * M + i
-                    sl, cw = bm.append_tokens(s, int(sufs[s]))
+                    n = int(sufs[s])
+                    # decode step: the continuation but its last token is in
+                    # the cache already (its copy-on-write pair is repeated
+                    # by the step); the last token is this step's
+                    sl, cw = bm.append_tokens(s, n if whole else n - 1)
+                    if not whole:
+                        slot, c1 = bm.append_token(s)
+                        sl = [slot]
+                        cw += [c1] if c1 else []
                     slots += sl
                     app_seq += [s] * len(sl)
                     cows += cw

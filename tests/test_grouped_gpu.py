@@ -51,11 +51,12 @@ def _tol(out_dtype, ref):
 
 
 # ------------------------------------------------------------------ the shared-prefix decode step
-@pytest.mark.parametrize("bs", [16, 32])
-def test_shared_prefix_step(gpu, bs):
-    """Forked samples of 4 prompts: CoW copy + continuation append, then grouped decode."""
+@pytest.mark.parametrize("bs,step", [(16, "decode"), (16, "continuation"), (32, "decode"), (32, "continuation")])
+def test_shared_prefix_step(gpu, bs, step):
+    """Forked samples of 4 prompts: CoW copy + append (one token per sample, or
+    each sample's whole continuation), then grouped decode."""
     wl = W.make_workload("shared_prefix", groups=4, per_group=16, prefix=512, suffix=(32, 300), seed=21,
-                         block_size=bs)
+                         block_size=bs, step=step)
     wl.poison()
     dev, dt = gpu, wl.dtype
     kc, vc = to_dev(wl.k_cache, dt, dev), to_dev(wl.v_cache, dt, dev)
@@ -75,13 +76,15 @@ def test_shared_prefix_step(gpu, bs):
 
 
 @pytest.mark.slow
-def test_full_size_step_sampled(gpu):
-    """The shared-prefix step the benchmark times, at full size (16 groups x 16
-    members, 1024-token prompt, 256 sequences): copy-on-write, the 68k-token
-    append, then the grouped call with its automatic partitions.  The pools
-    are compared bit for bit; outputs are sampled against the oracle (every
-    group's first and last member, plus random rows)."""
-    wl = W.make_workload("shared_prefix")
+@pytest.mark.parametrize("name", ["shared_prefix", "shared_prefix_prefill"])
+def test_full_size_step_sampled(gpu, name):
+    """The shared-prefix steps the benchmark times, at full size (16 groups x
+    16 members, 1024-token prompt, 256 sequences): the 240 copy-on-write
+    copies, the append (256 tokens, or the 68k-token continuation), then the
+    grouped call with its automatic partitions.  The pools are compared bit
+    for bit; outputs are sampled against the oracle (every group's first and
+    last member, plus random rows)."""
+    wl = W.make_workload(name)
     dev, dt = gpu, wl.dtype
     kc, vc = to_dev(wl.k_cache, dt, dev), to_dev(wl.v_cache, dt, dev)
     pkv.copy_blocks(kc, vc, _dev(wl.cow_pairs, dev))

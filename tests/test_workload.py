@@ -174,6 +174,30 @@ def test_shared_prefix_workload():
     assert not set(wl.cow_pairs[:, 1].tolist()) & set(wl.cow_pairs[:, 0].tolist())
     _check_slots(wl)
     assert wl.unique_kv_bytes() < wl.kv_bytes()
+    # the decode step: one new token per sample, at its last position, in a
+    # block of its own (never a shared one and never a copy destination)
+    assert len(wl.slot_mapping) == 256 and np.array_equal(wl.append_seq, np.arange(256))
+    for s in range(wl.num_seqs):
+        L = int(wl.context_lens[s])
+        blk = int(wl.block_tables[s, (L - 1) // 16])
+        assert wl.slot_mapping[s] == blk * 16 + (L - 1) % 16
+        others = np.delete(wl.block_tables, s, axis=0)
+        assert blk not in others and blk not in wl.cow_pairs[:, 1]
+
+
+def test_shared_prefix_prefill_workload():
+    """The same batch, with each sample's whole continuation written by the step."""
+    a = W.make_workload("shared_prefix", with_data=False)
+    b = W.make_workload("shared_prefix_prefill", with_data=False)
+    assert np.array_equal(a.context_lens, b.context_lens) and np.array_equal(a.block_tables, b.block_tables)
+    assert np.array_equal(a.cow_pairs, b.cow_pairs)
+    # every token past the prompt (1024 + t_g tokens per group) is appended
+    tails = np.repeat(W.uniform_ints(b.seed, W.S_GROUP, 16, 1, 15), 16)
+    assert len(b.slot_mapping) == int((b.context_lens - 1024 - tails).sum()) > 60000
+    # the decode step's slots are the continuation's last slots
+    last = {int(s): int(sl) for s, sl in zip(b.append_seq, b.slot_mapping)}
+    assert all(last[s] == a.slot_mapping[s] for s in range(256))
+    _check_slots(b)
 
 
 def test_long_context_workload_metadata():
