@@ -304,12 +304,21 @@ def _sample(wl, n, seed=0):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,nsample", [("llama8b", 48), ("opt13b", 48), ("shared_prefix", 48),
-                                          ("llama70b_long", 6)])
-def test_full_size_sampled(gpu, name, nsample):
-    """BASELINE sizes, in the launch configuration the benchmark times (auto partition)."""
+@pytest.mark.parametrize("name,nsample,fused", [
+    ("llama8b", 48, False), ("llama8b", 48, True), ("opt13b", 48, False), ("opt13b", 48, True),
+    ("shared_prefix", 48, False), ("shared_prefix_prefill", 48, False),
+    ("llama70b_long", 6, False), ("llama70b_long", 6, True)])
+def test_full_size_sampled(gpu, name, nsample, fused):
+    """The full-size workloads with the automatic partition; fused: the single
+    block-write + decode launch the benchmark times for one-token steps."""
     wl = W.make_workload(name)
-    kc, vc, out = gpu_step(wl, gpu)
+    if fused:
+        # the benchmark's partition choice for these shapes on one GB300
+        want = {"llama8b": 1024, "opt13b": 4096, "llama70b_long": 4096}[name]
+        if torch.cuda.get_device_properties(gpu).multi_processor_count == 152:
+            assert pkv.paged_attention_partition_size(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads,
+                                                      wl.max_context_len) == want
+    kc, vc, out = gpu_step(wl, gpu, fused=fused)
     sel = _sample(wl, nsample)
     okc, ovc, ref = oracle_step(wl, select=sel, in_place=True)
     # the step's writes, bit-exact; the rest of the pool untouched

@@ -50,6 +50,28 @@ def test_swap_out_and_in_bit_exact(gpu, layers):
     assert pkv.check_device_error() == 0
 
 
+@pytest.mark.parametrize("layers", [3, 33])
+def test_copy_blocks_every_layer_bit_exact(gpu, layers):
+    """Batched copy-on-write copy over several layers' pools in one call (33
+    layers: more than one launch's 32).  Every layer's K and V pools must equal
+    the oracle's copy of that layer, byte for byte; blocks outside the pairs
+    keep their bytes."""
+    rng = np.random.default_rng(100 + layers)
+    nb, hkv, bs, d = 40, 8, 16, 128
+    perm = rng.permutation(nb)
+    pairs = np.stack([perm[:9], perm[9:18]], axis=1).astype(np.int64)  # distinct dsts, none of them a src
+    bits = [W.normal(layers, 50 + l, (nb, hkv, bs, d), "bf16") for l in range(2 * layers)]
+    ks = [to_dev(bits[2 * l], "bf16", gpu) for l in range(layers)]
+    vs = [to_dev(bits[2 * l + 1], "bf16", gpu) for l in range(layers)]
+    pkv.copy_blocks(ks, vs, torch.from_numpy(pairs).to(gpu))
+    torch.cuda.synchronize()
+    assert pkv.check_device_error() == 0
+    for l in range(layers):
+        ek, ev = bits[2 * l].copy(), bits[2 * l + 1].copy()
+        assert oracle.copy_blocks(ek, ev, pairs) == 0
+        assert np.array_equal(to_bits(ks[l]), ek) and np.array_equal(to_bits(vs[l]), ev), f"layer {l}"
+
+
 def test_swapped_sequence_decodes_the_same(gpu):
     """Swap a workload's sequences out to host memory and back into other blocks: same output bits."""
     wl = W.make_workload("llama8b", num_seqs=4, lens=("uniform", 300, 1500), seed=9)
