@@ -26,7 +26,10 @@ static int* error_word() {
     std::lock_guard<std::mutex> lock(g_err_mutex);
     if (!g_err_ptr[dev]) {
         void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_pkv_error) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_pkv_error) != cudaSuccess) {
+            (void)cudaGetLastError();  // reported as PKV_ERR_CUDA; leave no sticky error behind
+            return nullptr;
+        }
         g_err_ptr[dev] = static_cast<int*>(ptr);
     }
     return g_err_ptr[dev];

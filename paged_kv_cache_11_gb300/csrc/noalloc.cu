@@ -44,7 +44,10 @@ static void* static_workspace() {
     std::lock_guard<std::mutex> lock(g_static_ws_mutex);
     if (!g_static_ws_ptr[dev]) {
         void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_pkv_static_workspace) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_pkv_static_workspace) != cudaSuccess) {
+            (void)cudaGetLastError();  // the caller reports PKV_ERR_CUDA; leave no sticky error behind
+            return nullptr;
+        }
         g_static_ws_ptr[dev] = ptr;
     }
     return g_static_ws_ptr[dev];
