@@ -168,8 +168,9 @@ int32_t paged_attention_partition_size(int32_t num_seqs, int32_t num_q_heads, in
  * out:             [num_seqs][num_q_heads][head_dim] of out_dtype (PKV_FP32,
  *                  PKV_BF16 or PKV_FP16), 16-byte aligned.
  * partition_size:  tokens per split-K partition, a multiple of block_size;
- *                  0 picks 512, 1024 or 2048 from the amount of work and the
- *                  device's SM count.  When max_context_len > partition_size
+ *                  0 picks 512, 1024, 2048 or 4096 from the amount of work
+ *                  and the device's SM count (the largest that still gives
+ *                  every resident decode CTA two work units).  When max_context_len > partition_size
  *                  each partition writes (o_p, lse_p) to the workspace and
  *                  they are merged through their log-sum-exp: by the last
  *                  partition of each (sequence, head group) to finish when a
@@ -363,6 +364,12 @@ pkv_status compact_tokens(const int64_t* src_slots, const int64_t* dst_slots, in
  * an error since the last check, PKV_ERR_DEVICE_METADATA with the first
  * PKV_DEVERR_* code otherwise, or PKV_ERR_CUDA.  first_error_code may be
  * NULL.
+ * The word is one per device, shared by the library's calls on every stream,
+ * and only `stream` is synchronised: an error recorded by a kernel still
+ * running on another stream is not seen by this check, and is reported by a
+ * later one (or, if it lands between the read and the clear, lost).  To check
+ * the calls of several streams, synchronise all of them (or the device)
+ * before calling this.
  */
 pkv_status pkv_check_device_error(void* stream, int32_t* first_error_code);
 

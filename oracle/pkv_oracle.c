@@ -29,8 +29,7 @@
  *            blocks, the first N_max - 1 of them, leaving shared blocks
  *            intact).
  *
- * Readings where the pages leave a point open (each also listed in the
- * design notes):
+ * Readings where the pages leave a point open:
  *   - cache layout: k_cache and v_cache are [num_blocks][num_kv_heads]
  *     [block_size][head_dim], row-major; token position t of a sequence lives
  *     in logical block t / block_size at offset t % block_size;

@@ -18,7 +18,8 @@ LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libpagedkv.so"
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA, PKV_ERR_DEVICE_METADATA = range(6)
 PKV_BF16, PKV_FP16, PKV_FP32 = 0, 1, 2
-DEVERR_NAMES = {0: "none", 1: "slot", 2: "copy_id", 3: "context_len", 4: "block_id", 5: "timeout"}
+DEVERR_NAMES = {0: "none", 1: "slot", 2: "copy_id", 3: "context_len", 4: "block_id", 5: "timeout",
+                6: "prefix_len", 7: "group"}
 
 _DTYPE_CODE = {torch.bfloat16: PKV_BF16, torch.float16: PKV_FP16, torch.float32: PKV_FP32}
 
