@@ -48,6 +48,8 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = ROOT / "profiles" / "traffic_per_launch.txt"
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
+WARM_GPU_S = 0.5      # GPU time of warm-up steps run right before each timed region
+STAT_MIN_STEPS = 50   # per-step timings behind the median / p10 / p90
 
 
 def parse_args(argv=None):
@@ -66,6 +68,11 @@ def parse_args(argv=None):
     ap.add_argument("--unfused", action="store_true", help="separate block-write and decode launches")
     ap.add_argument("--ungrouped", action="store_true",
                     help="shared-prefix workloads: plain paged_attention_decode instead of the grouped call")
+    ap.add_argument("--warm-ms", type=float, default=WARM_GPU_S * 1e3,
+                    help="GPU time of extra warm-up steps run right before each timed region (0: none, e.g. under "
+                         "a profiler)")
+    ap.add_argument("--stat-steps", type=int, default=STAT_MIN_STEPS,
+                    help="steps of the per-step statistics run (at least --steps; 0: skip it)")
     ap.add_argument("--flush-l2", action="store_true",
                     help="write a 256 MB buffer before every step (outside the step's timing) so that no step "
                          "finds the previous one's K/V in L2")
@@ -330,10 +337,6 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- our arm
-WARM_GPU_S = 0.5      # GPU time of warm-up steps run right before each timed region
-STAT_MIN_STEPS = 50   # per-step timings behind the median / p10 / p90
-
-
 def percentiles(xs) -> dict:
     a = np.sort(np.asarray(xs, dtype=np.float64))
     return {"median_ms": float(np.median(a)), "p10_ms": float(np.percentile(a, 10)),
@@ -433,7 +436,7 @@ def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool)
     torch.cuda.synchronize()
     assert pkv.check_device_error() == 0, "device error during warm-up"
     warm_ms, batch = 0.0, 8
-    while warm_ms < 1e3 * WARM_GPU_S:
+    while warm_ms < args.warm_ms:
         a, b = event_pair()
         a.record(stream)
         for _ in range(batch):
@@ -442,7 +445,7 @@ def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool)
         b.synchronize()
         ms = a.elapsed_time(b)
         warm_ms += ms
-        batch = int(min(4096, max(batch, batch * 1e3 * WARM_GPU_S / max(ms, 1e-3) / 4)))
+        batch = int(min(4096, max(batch, batch * args.warm_ms / max(ms, 1e-3) / 4)))
 
     # ---- the timed region: exactly args.steps steps.  A step that is one
     # launch (the fused decode) runs back to back between two events, so
@@ -486,7 +489,7 @@ def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool)
     # bracket the decode call of a multi-launch step).  An event between two
     # launches keeps the next one from starting while the previous one
     # drains, so these times run slightly above the timed region's mean.
-    n_stat = max(STAT_MIN_STEPS, args.steps)
+    n_stat = max(args.stat_steps, args.steps) if args.stat_steps > 0 else 0
     st_evs = [event_pair() for _ in range(n_stat)]
     dec_evs = [event_pair() for _ in range(n_stat)] if not fused else None
     for i in range(n_stat):
@@ -496,11 +499,13 @@ def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool)
     torch.cuda.synchronize()
     if d.clocks:
         d.clocks.mark(False)
-    stats = percentiles([a.elapsed_time(b) for a, b in st_evs])
-    stats["how"] = ("each of %d steps bracketed by its own CUDA events on the launching stream (run after the "
-                    "timed region; the events keep consecutive launches from overlapping)" % n_stat)
-    if dec_evs:
-        stats["decode_call"] = percentiles([a.elapsed_time(b) for a, b in dec_evs])
+    stats = None
+    if n_stat:
+        stats = percentiles([a.elapsed_time(b) for a, b in st_evs])
+        stats["how"] = ("each of %d steps bracketed by its own CUDA events on the launching stream (run after "
+                        "the timed region; the events keep consecutive launches from overlapping)" % n_stat)
+        if dec_evs:
+            stats["decode_call"] = percentiles([a.elapsed_time(b) for a, b in dec_evs])
     assert pkv.check_device_error() == 0
 
     # ---- end to end: host buffers in, result out, through the public API.

@@ -61,7 +61,12 @@ static EncodeTiledFn encode_fn() {
 // KV head) tile.  Rank 3: the same memory as [2 halves][rows][64], the two
 // halves of a row 128 bytes apart, box [2][BS][64]: one copy brings the
 // whole tile as its two halves back to back, the layout the rank-2 copies
-// of both halves give.  Every coordinate stays inside the pool.  No L2
+// of both halves give.  Rank 4: the same memory as [rows / 8 groups][2
+// halves][8 rows][64], box [BS / 8][2][8][64]: one copy brings the whole
+// tile as 8-row groups of 2 KiB, each holding both halves of its 8 rows, so
+// that tiles copied back to back keep every half's 8-row groups 2 KiB apart
+// across tile boundaries (the layout the prefix kernel's 128-token tensor
+// core operands need).  Every coordinate stays inside the pool.  No L2
 // promotion: every copy is a whole contiguous tile half or tile, and
 // promotion to 256-byte lines measured slightly slower on decode.
 static pkv_status encode_cache_map(CUtensorMap* m, const void* base, const pkv_cache_desc& c, int rank) {
@@ -78,11 +83,18 @@ static pkv_status encode_cache_map(CUtensorMap* m, const void* base, const pkv_c
         const cuuint32_t box[2] = {64, (cuuint32_t)c.block_size};
         r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
+    } else if (rank == 3) {
         const cuuint64_t dims[3] = {64, rows, 2};
         const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, 128};
         const cuuint32_t box[3] = {64, (cuuint32_t)c.block_size, 2};
         r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint32_t estr4[4] = {1, 1, 1, 1};
+        const cuuint64_t dims[4] = {64, 8, 2, rows / 8};  // block_size is a multiple of 8
+        const cuuint64_t strides[3] = {(cuuint64_t)kHeadDim * 2, 128, (cuuint64_t)kHeadDim * 2 * 8};
+        const cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)c.block_size / 8};
+        r = fn(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr4, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_INVALID_ARG;
@@ -389,15 +401,17 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
 
     int* err = error_word();
     if (!err) return PKV_ERR_CUDA;
-    // whole tiles (rank 3) for the decode kernel and for V in the prefix
-    // kernel; the prefix kernel's K chunks need one copy per dims half (rank 2)
-    CUtensorMap tmk, tmv, tmk_half;
+    // whole tiles: halves back to back (rank 3) for the decode kernel, 8-row
+    // groups (rank 4) for the prefix kernel
+    CUtensorMap tmk, tmv, tmk4, tmv4;
     st = encode_cache_map(&tmk, k_cache, *cache, 3);
     if (st != PKV_OK) return st;
     st = encode_cache_map(&tmv, v_cache, *cache, 3);
     if (st != PKV_OK) return st;
     if (grp) {
-        st = encode_cache_map(&tmk_half, k_cache, *cache, 2);
+        st = encode_cache_map(&tmk4, k_cache, *cache, 4);
+        if (st != PKV_OK) return st;
+        st = encode_cache_map(&tmv4, v_cache, *cache, 4);
         if (st != PKV_OK) return st;
     }
 
@@ -455,7 +469,7 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
     int launches = 0;
     cudaError_t e = cudaSuccess;
     if (grp && prefix_parts > 0 && grp->num_groups > 0)
-        e = launch_group_prefix(p, cache->dtype, cache->block_size, tmk_half, tmv, static_cast<cudaStream_t>(stream),
+        e = launch_group_prefix(p, cache->dtype, cache->block_size, tmk4, tmv4, static_cast<cudaStream_t>(stream),
                                 &launches);
     if (e == cudaSuccess)
         e = launch_decode(p, cache->dtype, cache->block_size, tmk, tmv, static_cast<cudaStream_t>(stream), &launches);

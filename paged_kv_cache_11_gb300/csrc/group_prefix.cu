@@ -1,5 +1,6 @@
 // group_prefix.cu -- the shared-prefix half of grouped decode, on the
-// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+// 5th-generation tensor cores (tcgen05, operands and accumulators in tensor
+// memory).
 //
 // Sequences forked from one prompt (parallel samples, beams, a common
 // system prompt) hold the prompt's K/V in the same physical blocks: the
@@ -18,42 +19,47 @@
 //
 // With up to 64 query rows per shared tile this is a dense contraction, so
 // both products run as tcgen05.mma.kind::f16 with fp32 accumulators in
-// tensor memory (TMEM), M = 128 rows:
-//   S = Q K^T   A = Q [128 rows x 128 dims], B = K [64 tokens x 128 dims],
-//               both K-major, 128-byte swizzle      -> TMEM columns [0, 64) or [64, 128)
-//   O += P V    A = P [128 rows x 64 tokens] (K-major), B = V [64 tokens x
-//               128 dims] read dims-major (MN-major), 16 tokens per product
-//               (within one block)                   -> TMEM columns [128, 256)
-// The tile's 64 query rows are fed twice as Q (rows r and r + 64 of A), so
-// TMEM lanes r and r + 64 hold the same row of S: thread r takes the first
-// 32 tokens of each chunk, thread r + 64 the other 32, and the two exchange
-// their maxima and sums.  P keeps ~16 significant bits as a 16-bit high part
-// plus a 16-bit residual: row r of P's A operand is the high part of query
-// row r and row r + 64 its residual, so one product accumulates both, in
-// lanes r and r + 64 of O, which the epilogue adds.  (A tcgen05.mma with
-// M = 128 costs the tensor core about the same time for any N up to 64 and
-// about a third more at 128, so the rows a product carries matter more
-// than its width.)
+// tensor memory (TMEM), M = 128 rows, 128 tokens per chunk:
+//   S = Q K^T   A = Q from TMEM [128 rows x 128 dims], B = K from shared
+//               memory [128 tokens x 128 dims], K-major, 128-byte swizzle,
+//               N = 128                              -> TMEM columns [0, 128) or [128, 256)
+//   O += P V    A = P from TMEM [128 rows x 128 tokens], B = V from shared
+//               memory read dims-major (MN-major), 16 tokens per product
+//                                                    -> TMEM columns [256, 384)
+// The tile's 64 query rows are held twice as Q (TMEM lanes r and r + 64), so
+// lanes r and r + 64 hold the same row of S: thread r takes the first 64
+// tokens of each chunk, thread r + 64 the other 64, and the two exchange
+// their maxima.  P keeps ~16 significant bits as a 16-bit high part plus a
+// 16-bit residual: lane r of P holds the high part of query row r and lane
+// r + 64 its residual, so one product accumulates both, in lanes r and r + 64
+// of O, which the epilogue adds.  Each thread packs the high and residual
+// parts of its own 64 tokens; the pair swaps the halves that belong in the
+// other's lane through shared memory and writes P over the S columns it was
+// computed from.  With Q and P in TMEM the products read only K and V from
+// shared memory, whose bandwidth (128 bytes per cycle) otherwise sets the
+// pace of a product with N <= 128.
 //
-// The partition streams through in chunks of 64 tokens, pipelined across
+// Shared-memory layout of a chunk: each (block, KV head) tile of K or V
+// lands in one TMA copy as 8-token groups of 2 KiB (the two 64-dim halves of
+// the 8 rows back to back, 128-byte swizzle), tile after tile, so that the
+// 8-token groups of the whole chunk sit 2 KiB apart across block boundaries
+// and one descriptor spans 128 tokens.
+//
+// The partition streams through in chunks of 128 tokens, pipelined across
 // three roles that hand off on mbarriers:
-//   TMA warp: the chunk's (block, KV head) tiles of K and V into a 5-stage
-//     ring.  K lands as two [64 tokens][64 dims] halves, tokens contiguous
-//     across the chunk's blocks (one copy per block and half); V lands tile
-//     after tile, each as its two [BS][64] halves (one copy per tile).  The
-//     copies of a chunk are issued from separate lanes;
+//   TMA warp: the chunk's tiles of K and V into a 3-stage ring (one copy per
+//     tile and tensor, issued from separate lanes);
 //   MMA warp (one thread): S(c+1) = Q K(c+1)^T into the other S buffer while
-//     the softmax works on chunk c, then O += P(c) V(c) once P(c) is written;
-//     each product's completion is signalled by tcgen05.commit;
+//     the softmax works on chunk c, then O += P(c) V(c) once P(c) is in
+//     TMEM; each product's completion is signalled by tcgen05.commit;
 //   softmax warps 0-3 (TMEM lanes 0-127): S(c) from TMEM, the online softmax
 //     in the log2 domain with the running max raised lazily (as in the decode
-//     warp core; O and l are rescaled when it is), P(c) into shared memory
-//     once the previous chunk's product has read it, and at the end the
-//     normalised output and log-sum-exp.
+//     warp core; O and l are rescaled when it is), P(c) into TMEM, and at the
+//     end the normalised output and log-sum-exp.
 // Every wait is bounded; a wait that runs out records PKV_DEVERR_TIMEOUT.
-// The softmax warps then stop together at the next chunk and the other roles
-// at their next wait; the copies and products already issued are waited for
-// (bounded) before the CTA frees its tensor memory or exits.
+// The softmax warps then stop together at their next barrier and the other
+// roles at their next wait; the copies and products already issued are
+// waited for (bounded) before the CTA frees its tensor memory or exits.
 #include "decode_common.cuh"
 
 namespace pkv {
@@ -62,12 +68,12 @@ constexpr int kSoftWarps = 4;             // TMEM lanes 0-127
 constexpr int kTmaWarp = kSoftWarps;      // K/V loads
 constexpr int kMmaWarp = kSoftWarps + 1;  // tensor-core products (lane 0)
 constexpr int kPrefixThreads = (kSoftWarps + 2) * 32;
-constexpr int kChunk = 64;                // tokens per pipeline step
+constexpr int kChunk = 128;               // tokens per pipeline step
 constexpr int kUmmaM = 128;               // M of both products
-constexpr int kRing = 5;                  // K/V chunks in flight
-constexpr int kPBufs = 1;                 // P buffers (a chunk's P waits for the product kPBufs chunks back)
-constexpr uint32_t kTmemCols = 256;       // S: [0, 64) and [64, 128); O: [128, 256)
-constexpr uint32_t kOCol = 128;
+constexpr int kRing = 3;                  // K/V chunks in flight
+constexpr uint32_t kTmemCols = 512;       // S: [0, 128), [128, 256); O: [256, 384); Q: [384, 448)
+constexpr uint32_t kOCol = 256;
+constexpr uint32_t kQCol = 384;
 
 // ---- tcgen05 wrappers (PTX ISA: tcgen05 instructions, shared memory and
 // instruction descriptors)
@@ -88,12 +94,14 @@ __device__ __forceinline__ uint32_t umma_idesc(bool bf16, int M, int N, bool a_m
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D (TMEM) = A B^T (+ D when accumulate); issued by one thread.
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, int accumulate) {
+// D (TMEM) = A B^T (+ D when accumulate), A in TMEM (row i in lane i, two
+// 16-bit elements of K per 32-bit column), B in shared memory; one thread.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            int accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -114,10 +122,9 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {  /
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
-// 32w .. 32w+31); every lane of the warp executes it.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
+// 32 consecutive 32-bit columns of this thread's TMEM lane (warp w reads
+// lanes 32w .. 32w+31); every lane of the warp executes it.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
         "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -127,57 +134,54 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    tmem_ld32(taddr, r);
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// The reverse: 32 fp32 columns of this thread's lane from registers.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+// The reverse: 32 columns of this thread's lane from registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
         "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+    tmem_st32(taddr, r);
+}
 
 // Barrier over the softmax warps only (named barrier 1).
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftWarps * 32) : "memory"); }
 
 // Barrier over the softmax warps and the MMA warp, not the TMA warp (named
-// barrier 2): Q is in shared memory and the TMEM columns are allocated.
+// barrier 2).
 __device__ __forceinline__ void compute_sync() {
     asm volatile("bar.sync 2, %0;" ::"n"((kSoftWarps + 1) * 32) : "memory");
 }
 
-// Byte offset of 16-byte chunk c (0-7) of row r in a [rows][64 x 16-bit]
-// region with the 128-byte swizzle (the layout TMA writes and the
-// descriptors above read).
-__device__ __forceinline__ uint32_t sw128_chunk(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
-
 struct PrefixSmem {
-    static constexpr int kQHalf = kUmmaM * 128;   // Q: [128 rows][64 dims] per dims half, 16 KiB
-    static constexpr int kKVHalf = kChunk * 128;  // a chunk of K or V: [64 tokens][64 dims] per dims half, 8 KiB
-    static constexpr int kPBuf = kUmmaM * 128;    // P: [128 rows][64 tokens], 16 KiB per buffer
-    static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQOff + 2 * kQHalf;
-    static constexpr int kVOff = kKOff + kRing * 2 * kKVHalf;
-    static constexpr int kPOff = kVOff + kRing * 2 * kKVHalf;
-    static constexpr int kBarOff = kPOff + kPBufs * kPBuf;
-    // kvfull[kRing], kvempty[kRing], sfull[2], sfree[2], pfull[kPBufs], pvdone[kPBufs]
-    static constexpr int kNumBars = 2 * kRing + 4 + 2 * kPBufs;
+    static constexpr int kStage = kChunk * kHeadDim * 2;  // a chunk of K or V: 128 tokens x 128 dims, 32 KiB
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kKOff + kRing * kStage;
+    // the pair exchange of P: [8 chunks of 16 bytes][128 threads]
+    static constexpr int kXOff = kVOff + kRing * kStage;
+    static constexpr int kXBytes = 8 * kUmmaM * 16;
+    static constexpr int kBarOff = kXOff + kXBytes;
+    // kvfull[kRing], kvempty[kRing], sfull[2], pfull[2], pvdone
+    static constexpr int kNumBars = 2 * kRing + 5;
     static constexpr int kSlotOff = kBarOff + kNumBars * 8;
     // per member of the tile: sequence, prefix tokens (0 when it takes no
     // part), partitions in all, whether the prefix side merges; per (member,
@@ -186,11 +190,12 @@ struct PrefixSmem {
     static constexpr int kMemBytes = kPrefixRows * 4 * 4 + kPrefixRows * 4 * 4;
     static constexpr int kXchOff = kMemOff + kMemBytes;  // [2][128] chunk maxima, [128] row sums
     static constexpr int kFlagOff = kXchOff + 3 * kUmmaM * 4;
-    static constexpr int kTotal = kFlagOff + 16;
+    static constexpr int kTotal = kFlagOff + 32;
     static constexpr int kDynamic = kTotal + 1024;  // slack to align the base to 1024 B
     // epilogue: every lane's O row, [128][kRedStride] floats over the K/V ring
     static constexpr int kRedOff = kKOff;
-    static_assert(kUmmaM * kRedStride * 4 <= 2 * kRing * 2 * kKVHalf, "O rows fit the ring");
+    static_assert(kUmmaM * kRedStride * 4 <= 2 * kRing * kStage, "O rows fit the ring");
+    static_assert(kDynamic <= 227 * 1024, "shared memory of one CTA");
 };
 
 template <bool kBF16, int BS>
@@ -200,9 +205,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     using S = PrefixSmem;
     constexpr int D = kHeadDim;
     constexpr int kBlocksPerChunk = kChunk / BS;
-    static_assert(kChunk % BS == 0 && 3 * kBlocksPerChunk <= 32, "whole blocks per chunk, one copy per lane");
+    static_assert(kChunk % BS == 0 && BS % 8 == 0 && kBlocksPerChunk <= 16, "whole blocks per chunk, one copy per lane");
     static_assert(2 * kPrefixRows == kUmmaM && kSoftWarps * 32 == kUmmaM, "each row twice, one thread per TMEM lane");
-    static_assert(kPrefixRows * 16 % (kSoftWarps * 32) == 0, "whole Q loads per thread");
     static_assert(kPrefixPartitionMax / 16 <= 64, "a partition's block ids fit two registers per lane");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_sa = smem_addr(smem_raw);
@@ -227,16 +231,15 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     int* mem_arrive = mem_np + kPrefixRows;                   // [64] 1: the prefix side merges
     int* verdict = mem_arrive + kPrefixRows;                  // [64 * 4]
     // [0]: bad block id (bit 0) / a wait ran out (bit 1); [1]: tile token
-    // end; [2]: a softmax warp's wait ran out (read only after softmax_sync);
-    // [3]: some member's partials are merged on this side
+    // end; [2], [4]: a softmax warp's wait ran out, read by every softmax
+    // thread after the barrier that follows the wait ([2]: S, [4]: the
+    // previous product); [3]: some member's partials are merged on this side
     int* flags = reinterpret_cast<int*>(smem + S::kFlagOff);
     float* xch = reinterpret_cast<float*>(smem + S::kXchOff);
     const uint32_t bar0 = smem_addr(smem + S::kBarOff);
-    const uint32_t kvfull0 = bar0, kvempty0 = bar0 + 8 * kRing, sfull0 = bar0 + 16 * kRing, sfree0 = sfull0 + 16,
-                   pfull0 = sfree0 + 16, pvdone0 = pfull0 + 8 * kPBufs;
+    const uint32_t kvfull0 = bar0, kvempty0 = bar0 + 8 * kRing, sfull0 = bar0 + 16 * kRing, pfull0 = sfull0 + 16,
+                   pvdone = pfull0 + 16;
     const uint32_t slot = smem_addr(smem + S::kSlotOff);
-    uint8_t* const qreg = smem + S::kQOff;
-    uint8_t* const preg = smem + S::kPOff;
 
     const int gs0 = p.group_starts[g], gs1 = p.group_starts[g + 1];
     const bool bad_group = gs0 < 0 || gs1 < gs0 || gs1 > p.num_seqs;
@@ -250,22 +253,16 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         if (part == 0 && kvh == 0 && rt == 0 &&
             (bad_group || gs1 - gs0 > p.row_tiles * p.members_per_tile))
             record_error(p.err, PKV_DEVERR_GROUP);
-        flags[0] = 0;
-        flags[1] = 0;
-        flags[2] = 0;
-        flags[3] = 0;
+        for (int i = 0; i < 8; ++i) flags[i] = 0;
         for (int i = 0; i < kRing; ++i) {
             mbar_init(kvfull0 + 8 * i, 1);
             mbar_init(kvempty0 + 8 * i, 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(sfull0 + 8 * i, 1);
-            mbar_init(sfree0 + 8 * i, kSoftWarps);
-        }
-        for (int i = 0; i < kPBufs; ++i) {
             mbar_init(pfull0 + 8 * i, kSoftWarps);
-            mbar_init(pvdone0 + 8 * i, 1);
         }
+        mbar_init(pvdone, 1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -291,40 +288,41 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     const int nchunks = (ntok + kChunk - 1) / kChunk;
     const int rows = nmem * G;  // <= 64
 
-    // ---- TMEM (MMA warp), Q rows into shared memory (softmax warps).  The
-    // TMA warp needs neither and starts its copies at once.
+    // ---- TMEM (MMA warp) and Q (softmax warps: this lane's row, zeros past
+    // the tile's rows, into TMEM columns [kQCol, kQCol + 64)).  The TMA warp
+    // needs neither and starts its copies at once.
     if (warp == kMmaWarp) tmem_alloc(slot, kTmemCols);
+    uint32_t qa[32], qb[32];
     if (warp < kSoftWarps) {
-        // Q rows of the tile (row r: member r / G, head r % G of its KV head),
-        // zeros up to row 63, and again as rows 64-127.  Every load is
-        // issued before any is stored.
-        constexpr int kQPerThread = kPrefixRows * 16 / (kSoftWarps * 32);
-        uint4 qv[kQPerThread];
-#pragma unroll
-        for (int k = 0; k < kQPerThread; ++k) {
-            const int i = tid + k * kSoftWarps * 32, r = i >> 4, c = i & 15;
-            qv[k] = make_uint4(0, 0, 0, 0);
-            if (r < rows) {
-                const int mi = r / G;
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    static_cast<const uint16_t*>(p.q) + ((int64_t)mem_s[mi] * p.num_q_heads + kvh * G + r - mi * G) * D);
-                qv[k] = __ldg(src + c);
-            }
+        const int r = tid & (kPrefixRows - 1);
+        const uint4* src = nullptr;
+        if (r < rows) {
+            const int mi = r / G;
+            src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                 ((int64_t)mem_s[mi] * p.num_q_heads + kvh * G + r - mi * G) * D);
         }
 #pragma unroll
-        for (int k = 0; k < kQPerThread; ++k) {
-            const int i = tid + k * kSoftWarps * 32, r = i >> 4, c = i & 15;
-            *reinterpret_cast<uint4*>(qreg + (c >> 3) * S::kQHalf + sw128_chunk(r, c & 7)) = qv[k];
-            *reinterpret_cast<uint4*>(qreg + (c >> 3) * S::kQHalf + sw128_chunk(r + kPrefixRows, c & 7)) = qv[k];
+        for (int k = 0; k < 8; ++k) {
+            const uint4 a = src ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+            const uint4 b = src ? __ldg(src + 8 + k) : make_uint4(0, 0, 0, 0);
+            qa[4 * k] = a.x, qa[4 * k + 1] = a.y, qa[4 * k + 2] = a.z, qa[4 * k + 3] = a.w;
+            qb[4 * k] = b.x, qb[4 * k + 1] = b.y, qb[4 * k + 2] = b.z, qb[4 * k + 3] = b.w;
         }
-        fence_proxy_async_shared();  // the tensor cores read Q through the async proxy
     }
     uint32_t tmem = 0;
     if (warp != kTmaWarp) {
         tc_fence_before();
-        compute_sync();
+        compute_sync();  // the TMEM address is in shared memory
         tc_fence_after();
         tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kSlotOff);
+        if (warp < kSoftWarps) {
+            const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+            tmem_st32(lane_addr + kQCol, qa);       // dims 0-63, two per column
+            tmem_st32(lane_addr + kQCol + 32, qb);  // dims 64-127
+        }
+        tc_fence_before();
+        compute_sync();  // Q is in TMEM
+        tc_fence_after();
     }
 
     float m_run = -INFINITY;  // softmax threads: running max of the row (raised lazily)
@@ -364,26 +362,20 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                 break;
             }
             const uint32_t fb = kvfull0 + 8 * st;
-            const uint32_t kdst = smem_addr(smem + S::kKOff + st * 2 * S::kKVHalf);
-            const uint32_t vdst = smem_addr(smem + S::kVOff + st * 2 * S::kKVHalf);
-            if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)nb * BS * 128 * 4);
+            if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)nb * BS * D * 2 * 2);
             __syncwarp();
-            // one copy per lane, so that the copies of a chunk are issued side
-            // by side: lane 3b + w takes block b's K dims half w (w < 2; the
-            // chunk's tokens stay contiguous within each half) or its whole
-            // V tile (w = 2; the tile's two halves back to back)
-            {
-                const int b = lane / 3, w = lane - 3 * b;
-                const int j = (b0 + b) & 63;  // in range whenever b < nb
-                const int lo = __shfl_sync(0xffffffffu, ids[0], j & 31), hi = __shfl_sync(0xffffffffu, ids[1], j & 31);
-                const int pid = j < 32 ? lo : hi;
-                if (b < nb) {
-                    const int y = (pid * p.num_kv_heads + kvh) * BS;  // row of the tile in [rows][128]
-                    if (w < 2)
-                        tma_load_2d(kdst + w * S::kKVHalf + b * BS * 128, &tmk, fb, 64 * w, y, policy);
-                    else
-                        tma_load_3d(vdst + b * 2 * BS * 128, &tmv, fb, 0, y, 0, policy);
-                }
+            // lane b: block b's K tile; lane 16 + b: its V tile.  A tile lands
+            // as BS / 8 groups of 8 tokens x both dims halves (2 KiB each),
+            // tile after tile, so the chunk's 8-token groups are 2 KiB apart.
+            const int b = lane & 15;
+            const int j = (b0 + b) & 63;  // in range whenever b < nb
+            const int lo = __shfl_sync(0xffffffffu, ids[0], j & 31), hi = __shfl_sync(0xffffffffu, ids[1], j & 31);
+            const int pid = j < 32 ? lo : hi;
+            if (b < nb) {
+                const int grp = (pid * p.num_kv_heads + kvh) * (BS / 8);  // first 8-row group of the tile
+                const uint32_t dst = smem_addr(smem + (lane < 16 ? S::kKOff : S::kVOff) + st * S::kStage) +
+                                     b * BS * D * 2;
+                tma_load_4d(dst, lane < 16 ? &tmk : &tmv, fb, 0, 0, 0, grp, policy);
             }
             ++issued;
         }
@@ -399,49 +391,48 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
             uint32_t last_bar = 0, last_par = 0;  // the latest commit and its phase parity
             bool ok = true;
             for (int c = -1; c < nchunks && ok; ++c) {
-                // S(c+1) = Q K(c+1)^T into S buffer (c+1) & 1, ahead of the softmax
+                // S(c+1) = Q K(c+1)^T into S buffer (c+1) & 1, ahead of the
+                // softmax.  That buffer last held P(c-1), which PV(c-1),
+                // issued before this product, has read (the tensor core runs
+                // one thread's products in issue order).
                 const int cs = c + 1;
                 if (cs < nchunks) {
                     const int st = cs % kRing, sb = cs & 1;
-                    ok = mbar_wait(kvfull0 + 8 * st, (cs / kRing) & 1) &&
-                         (cs < 2 || mbar_wait(sfree0 + 8 * sb, ((cs >> 1) - 1) & 1));
+                    ok = mbar_wait(kvfull0 + 8 * st, (cs / kRing) & 1);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t kb = smem_addr(smem + S::kKOff + st * 2 * S::kKVHalf);
+                    const uint32_t kb = smem_addr(smem + S::kKOff + st * S::kStage);
                     const int nt = min(kChunk, ntok - cs * kChunk);  // a multiple of 16
                     const uint32_t id_s = umma_idesc(kBF16, kUmmaM, nt, false, false);
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t a = smem_addr(qreg + (ks >> 2) * S::kQHalf) + (ks & 3) * 32;
-                        const uint32_t b = kb + (ks >> 2) * S::kKVHalf + (ks & 3) * 32;
-                        umma_f16(tmem + sb * kChunk, umma_desc_sw128(a, 16, 1024), umma_desc_sw128(b, 16, 1024),
-                                 id_s, ks > 0);
+                        // dims 16 ks .. 16 ks + 15: half ks / 4 of each 8-token group
+                        const uint32_t b = kb + (ks >> 2) * 1024 + (ks & 3) * 32;
+                        umma_f16_ts(tmem + sb * kChunk, tmem + kQCol + 8 * ks, umma_desc_sw128(b, 16, 2048), id_s,
+                                    ks > 0);
                     }
                     umma_commit(sfull0 + 8 * sb);
                     last_bar = sfull0 + 8 * sb;
                     last_par = (cs >> 1) & 1;
                 }
                 if (c < 0) continue;
-                // O += P(c) V(c): rows 0-63 the high part, rows 64-127 the residual
-                const int pb = c % kPBufs;
-                ok = mbar_wait(pfull0 + 8 * pb, (c / kPBufs) & 1);
+                // O += P(c) V(c): lanes 0-63 the high part, lanes 64-127 the residual
+                const int sb = c & 1;
+                ok = mbar_wait(pfull0 + 8 * sb, (c >> 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 const int st = c % kRing;
-                const uint32_t vb = smem_addr(smem + S::kVOff + st * 2 * S::kKVHalf);
-                const uint32_t pa = smem_addr(preg + pb * S::kPBuf);
+                const uint32_t vb = smem_addr(smem + S::kVOff + st * S::kStage);
                 const int nk = min(kChunk, ntok - c * kChunk) / 16;
-                // V's tiles lie block after block, each as its two dims halves
-                // ([BS][64] apiece): 16 tokens start at row 16 ks of the chunk
-                for (int ks = 0; ks < nk; ++ks) {
-                    const uint32_t v0 = vb + (16 * ks / BS) * (2 * BS * 128) + (16 * ks % BS) * 128;
-                    umma_f16(tmem + kOCol, umma_desc_sw128(pa + ks * 32, 16, 1024),
-                             umma_desc_sw128(v0, BS * 128, 1024), id_o, c > 0 || ks > 0);
-                }
+                // 16 tokens = two 8-token groups (4 KiB); the dims halves of a
+                // group are 1 KiB apart, the groups 2 KiB
+                for (int ks = 0; ks < nk; ++ks)
+                    umma_f16_ts(tmem + kOCol, tmem + sb * kChunk + 8 * ks, umma_desc_sw128(vb + ks * 4096, 1024, 2048),
+                                id_o, c > 0 || ks > 0);
                 umma_commit(kvempty0 + 8 * st);
-                umma_commit(pvdone0 + 8 * pb);
-                last_bar = pvdone0 + 8 * pb;
-                last_par = (c / kPBufs) & 1;
+                umma_commit(pvdone);
+                last_bar = pvdone;
+                last_par = c & 1;
             }
             if (!ok) {
                 atomicOr(flags, 2);
@@ -453,32 +444,31 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     } else {
         // ------------------------------------------------------------ softmax
         const int r = tid & (kPrefixRows - 1);  // the tile row this thread works on
-        const int half = tid >> 6;              // 0: tokens 0-31 of a chunk, dims 0-63; 1: the rest
+        const int half = tid >> 6;              // 0: tokens 0-63 of a chunk; 1: tokens 64-127
         const int lim = r < rows ? min(ntok, mem_lim[r / G] - tok0) : 0;  // tokens row r attends (<= 0: none)
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
         const float sl2 = p.scale_log2;
+        uint4* xbuf = reinterpret_cast<uint4*>(smem + S::kXOff);  // [8][128]
         float l = 0.f;  // this half's share of the row sum
         bool ok = true;
-        // Wait for the product of chunk j (warp-uniform verdict).
-        auto pv_done = [&](int j) {
-            return __all_sync(0xffffffffu, mbar_wait(pvdone0 + 8 * (j % kPBufs), (j / kPBufs) & 1));
-        };
         for (int c = 0; c < nchunks; ++c) {
             const int sb = c & 1;
-            float v[32];
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(sfull0 + 8 * sb, (c >> 1) & 1));
+            float v[64];
+            ok = __all_sync(0xffffffffu, mbar_wait(sfull0 + 8 * sb, (c >> 1) & 1));
             if (ok) {
                 tc_fence_after();
-                tmem_ld32(lane_addr + sb * kChunk + 32 * half, v);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sfree0 + 8 * sb);
+                float a[32], b[32];
+                tmem_ld32(lane_addr + sb * kChunk + 64 * half, a);
+                tmem_ld32(lane_addr + sb * kChunk + 64 * half + 32, b);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = a[j], v[32 + j] = b[j];
+            } else if (lane == 0) {
+                flags[2] = 1;
             }
-            if (!ok && lane == 0) flags[2] = 1;
-            const int t0 = c * kChunk + 32 * half;  // partition token of v[0]
+            const int t0 = c * kChunk + 64 * half;  // partition token of v[0]
             float mx = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 64; ++j) {
                 v[j] = ok && t0 + j < lim ? v[j] * sl2 : -INFINITY;
                 mx = fmaxf(mx, v[j]);
             }
@@ -500,25 +490,41 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
             }
             const float ms = m_run == -INFINITY ? 0.f : m_run;
             l *= alpha;
-            uint32_t hi[16], lo[16];
+            // this thread's 64 tokens as 32 columns of high parts and 32 of
+            // residuals; it keeps the ones of its own lane (lane r: high,
+            // lane r + 64: residual) and hands the others to its partner:
+            // tokens 0-63's residual goes to lane r + 64, tokens 64-127's
+            // high part to lane r
+            uint32_t keep[32];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float p0 = exp2f(v[2 * e] - ms), p1 = exp2f(v[2 * e + 1] - ms);
-                l += p0 + p1;
-                float r0, r1;
-                hi[e] = pack2<kBF16>(p0, p1, r0, r1);
-                lo[e] = pack2<kBF16>(p0 - r0, p1 - r1);
+            for (int q = 0; q < 8; ++q) {
+                uint32_t send[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = 4 * q + i;
+                    const float p0 = exp2f(v[2 * e] - ms), p1 = exp2f(v[2 * e + 1] - ms);
+                    l += p0 + p1;
+                    float r0, r1;
+                    const uint32_t hw = pack2<kBF16>(p0, p1, r0, r1);
+                    const uint32_t lw = pack2<kBF16>(p0 - r0, p1 - r1);
+                    keep[e] = half ? lw : hw;
+                    send[i] = half ? hw : lw;
+                }
+                xbuf[q * kUmmaM + tid] = make_uint4(send[0], send[1], send[2], send[3]);
             }
-            // O is rescaled once the previous chunk's product is in it; the P
-            // buffer is reused once the product kPBufs chunks back has read it
+            // O is rescaled once the previous chunk's product is in it
             const bool rescale = c > 0 && __any_sync(0xffffffffu, alpha != 1.f);
-            if (rescale)
-                ok = pv_done(c - 1);
-            else if (c >= kPBufs)
-                ok = pv_done(c - kPBufs);
-            if (!ok) {
-                if (lane == 0) flags[2] = 1;  // the next softmax_sync stops every softmax warp
-                continue;
+            if (rescale && !__all_sync(0xffffffffu, mbar_wait(pvdone, (c - 1) & 1)) && lane == 0) flags[4] = 1;
+            softmax_sync();
+            if (flags[4]) {  // as flags[2]: written only before this barrier
+                ok = false;
+                break;
+            }
+            uint32_t recv[32];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint4 x = xbuf[q * kUmmaM + (tid ^ kPrefixRows)];
+                recv[4 * q] = x.x, recv[4 * q + 1] = x.y, recv[4 * q + 2] = x.z, recv[4 * q + 3] = x.w;
             }
             tc_fence_after();
             if (rescale) {
@@ -533,23 +539,15 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                     tmem_st32(oa, o);
                 }
             }
-            // tokens 32 half .. +31 (16-byte chunks 4 half .. +3): the high
-            // part into row r, the residual into row r + 64
-            uint8_t* pbuf = preg + (c % kPBufs) * S::kPBuf;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int cc = 4 * half + q;
-                *reinterpret_cast<uint4*>(pbuf + sw128_chunk(r, cc)) =
-                    make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
-                *reinterpret_cast<uint4*>(pbuf + sw128_chunk(r + kPrefixRows, cc)) =
-                    make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
-            }
-            fence_proxy_async_shared();  // the tensor cores read P through the async proxy
+            // P over this lane's S columns: lane r the high part of tokens
+            // 0-127, lane r + 64 the residual, two tokens per column
+            tmem_st32(lane_addr + sb * kChunk + (half ? 32 : 0), keep);  // this thread's tokens
+            tmem_st32(lane_addr + sb * kChunk + (half ? 0 : 32), recv);  // the partner's
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(pfull0 + 8 * (c % kPBufs));
+            if (lane == 0) mbar_arrive(pfull0 + 8 * sb);
         }
-        if (ok) ok = pv_done(nchunks - 1);
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(pvdone, (nchunks - 1) & 1));
         tc_fence_after();
         if (!ok && lane == 0) {
             atomicOr(flags, 2);
@@ -645,7 +643,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
             const int mi = u / p.head_tiles, ht = u - mi * p.head_tiles;
             __threadfence();
             merge_row_partials(p, mem_s[mi], kvh * G + ht * HT, min(HT, G - ht * HT), mem_np[mi],
-                               reinterpret_cast<float*>(smem));  // Q's region: free now
+                               reinterpret_cast<float*>(smem));  // the ring's start: free now
             __syncthreads();  // the scratch is reused by the next merge
         }
     }

@@ -89,7 +89,7 @@ struct DecodeParams {
 // smallest (which sizes the workspace) and the largest.
 constexpr int kPrefixPartition = 256;
 constexpr int kPrefixPartitionMax = 1024;
-// Resident prefix CTAs per SM (about 197 KiB of shared memory each).
+// Resident prefix CTAs per SM (about 213 KiB of shared memory and 512 TMEM columns each).
 constexpr int kPrefixCtasPerSm = 1;
 // Query rows of one prefix CTA (each fed twice to the prefix kernel's M = 128 products).
 constexpr int kPrefixRows = 64;
@@ -267,6 +267,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// 4-D tiled TMA load (coordinates innermost first), as tma_load_2d.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z,
+                                            int w, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
         : "memory");
 }
 
