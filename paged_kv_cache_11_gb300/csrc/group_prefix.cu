@@ -27,17 +27,18 @@
 //               memory read dims-major (MN-major), 16 tokens per product
 //                                                    -> TMEM columns [256, 384)
 // The tile's 64 query rows are held twice as Q (TMEM lanes r and r + 64), so
-// lanes r and r + 64 hold the same row of S: thread r takes the first 64
-// tokens of each chunk, thread r + 64 the other 64, and the two exchange
-// their maxima.  P keeps ~16 significant bits as a 16-bit high part plus a
-// 16-bit residual: lane r of P holds the high part of query row r and lane
-// r + 64 its residual, so one product accumulates both, in lanes r and r + 64
-// of O, which the epilogue adds.  Each thread packs the high and residual
-// parts of its own 64 tokens; the pair swaps the halves that belong in the
-// other's lane through shared memory and writes P over the S columns it was
-// computed from.  With Q and P in TMEM the products read only K and V from
-// shared memory, whose bandwidth (128 bytes per cycle) otherwise sets the
-// pace of a product with N <= 128.
+// lanes r and r + 64 hold the same row of S.  Eight softmax warps work on
+// the 128 lanes, two per lane (warps w and w + 4 may both access lanes
+// 32 (w % 4) .. +31): the four threads of a row take 32 tokens of each chunk
+// apiece and exchange their maxima.  P keeps ~16 significant bits as a
+// 16-bit high part plus a 16-bit residual: lane r of P holds the high part of
+// query row r and lane r + 64 its residual, so one product accumulates both,
+// in lanes r and r + 64 of O, which the epilogue adds.  Each thread packs the
+// high and residual parts of its own tokens; it swaps the half that belongs
+// in the other lane with its partner there through shared memory and writes
+// P over the S columns it was computed from.  With Q and P in TMEM the
+// products read only K and V from shared memory, whose bandwidth (128 bytes
+// per cycle) otherwise sets the pace of a product with N <= 128.
 //
 // Shared-memory layout of a chunk: each (block, KV head) tile of K or V
 // lands in one TMA copy as 8-token groups of 2 KiB (the two 64-dim halves of
@@ -52,10 +53,11 @@
 //   MMA warp (one thread): S(c+1) = Q K(c+1)^T into the other S buffer while
 //     the softmax works on chunk c, then O += P(c) V(c) once P(c) is in
 //     TMEM; each product's completion is signalled by tcgen05.commit;
-//   softmax warps 0-3 (TMEM lanes 0-127): S(c) from TMEM, the online softmax
-//     in the log2 domain with the running max raised lazily (as in the decode
-//     warp core; O and l are rescaled when it is), P(c) into TMEM, and at the
-//     end the normalised output and log-sum-exp.
+//   softmax warps 0-7 (TMEM lanes 0-127, two warps per lane quarter): S(c)
+//     from TMEM, the online softmax in the log2 domain with the running max
+//     raised lazily (as in the decode warp core; O and l are rescaled when it
+//     is), P(c) into TMEM, and at the end the normalised output and
+//     log-sum-exp, written a row at a time through shared memory.
 // Every wait is bounded; a wait that runs out records PKV_DEVERR_TIMEOUT.
 // The softmax warps then stop together at their next barrier and the other
 // roles at their next wait; the copies and products already issued are
@@ -64,7 +66,7 @@
 
 namespace pkv {
 
-constexpr int kSoftWarps = 4;             // TMEM lanes 0-127
+constexpr int kSoftWarps = 8;             // two per TMEM lane quarter: warps w and w + 4 share lanes 32 (w % 4) ..
 constexpr int kTmaWarp = kSoftWarps;      // K/V loads
 constexpr int kMmaWarp = kSoftWarps + 1;  // tensor-core products (lane 0)
 constexpr int kPrefixThreads = (kSoftWarps + 2) * 32;
@@ -156,6 +158,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
     uint32_t r[32];
 #pragma unroll
@@ -176,9 +188,9 @@ struct PrefixSmem {
     static constexpr int kStage = kChunk * kHeadDim * 2;  // a chunk of K or V: 128 tokens x 128 dims, 32 KiB
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kKOff + kRing * kStage;
-    // the pair exchange of P: [8 chunks of 16 bytes][128 threads]
+    // the pair exchange of P: [4 chunks of 16 bytes][256 softmax threads]
     static constexpr int kXOff = kVOff + kRing * kStage;
-    static constexpr int kXBytes = 8 * kUmmaM * 16;
+    static constexpr int kXBytes = 4 * kSoftWarps * 32 * 16;
     static constexpr int kBarOff = kXOff + kXBytes;
     // kvfull[kRing], kvempty[kRing], sfull[2], pfull[2], pvdone
     static constexpr int kNumBars = 2 * kRing + 5;
@@ -188,13 +200,14 @@ struct PrefixSmem {
     // head tile): merge verdict
     static constexpr int kMemOff = kSlotOff + 16;
     static constexpr int kMemBytes = kPrefixRows * 4 * 4 + kPrefixRows * 4 * 4;
-    static constexpr int kXchOff = kMemOff + kMemBytes;  // [2][128] chunk maxima, [128] row sums
-    static constexpr int kFlagOff = kXchOff + 3 * kUmmaM * 4;
+    // [2][256] chunk maxima, [256] row sums (one per softmax thread)
+    static constexpr int kXchOff = kMemOff + kMemBytes;
+    static constexpr int kFlagOff = kXchOff + 3 * kSoftWarps * 32 * 4;
     static constexpr int kTotal = kFlagOff + 32;
     static constexpr int kDynamic = kTotal + 1024;  // slack to align the base to 1024 B
-    // epilogue: every lane's O row, [128][kRedStride] floats over the K/V ring
+    // epilogue: the residual lanes' O rows, [64][kRedStride] floats over the K/V ring
     static constexpr int kRedOff = kKOff;
-    static_assert(kUmmaM * kRedStride * 4 <= 2 * kRing * kStage, "O rows fit the ring");
+    static_assert(kPrefixRows * kRedStride * 4 <= 2 * kRing * kStage, "O rows fit the ring");
     static_assert(kDynamic <= 227 * 1024, "shared memory of one CTA");
 };
 
@@ -206,7 +219,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     constexpr int D = kHeadDim;
     constexpr int kBlocksPerChunk = kChunk / BS;
     static_assert(kChunk % BS == 0 && BS % 8 == 0 && kBlocksPerChunk <= 16, "whole blocks per chunk, one copy per lane");
-    static_assert(2 * kPrefixRows == kUmmaM && kSoftWarps * 32 == kUmmaM, "each row twice, one thread per TMEM lane");
+    static_assert(2 * kPrefixRows == kUmmaM && kSoftWarps * 32 == 2 * kUmmaM,
+                  "each row twice, two softmax threads per TMEM lane");
     static_assert(kPrefixPartitionMax / 16 <= 64, "a partition's block ids fit two registers per lane");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_sa = smem_addr(smem_raw);
@@ -266,6 +280,20 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         fence_barrier_init();
     }
     __syncthreads();
+    // The TMA warp loads the block ids of the partition from the group's
+    // first member's table (block j in ids[j / 32] of lane j % 32) while the
+    // member metadata below is read; ids past the tile's token end (known
+    // after that) are not used.
+    int ids[2] = {0, 0};
+    if (warp == kTmaWarp && nmem > 0) {
+        const int32_t* table = p.block_tables + (int64_t)gs0 * p.max_blocks_per_seq + tok0 / BS;
+        const int jmax = min(p.prefix_partition / BS, p.max_blocks_per_seq - tok0 / BS);  // within the table row
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int j = 32 * k + lane;
+            if (j < jmax) ids[k] = __ldg(table + j);
+        }
+    }
     // Member metadata.  The first CTA of each row tile also records each
     // member's group (the decode kernel's hint, see group_verified).
     for (int i = tid; i < nmem; i += blockDim.x) {
@@ -292,21 +320,25 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     // the tile's rows, into TMEM columns [kQCol, kQCol + 64)).  The TMA warp
     // needs neither and starts its copies at once.
     if (warp == kMmaWarp) tmem_alloc(slot, kTmemCols);
-    uint32_t qa[32], qb[32];
+    // Softmax thread roles: warp w works on TMEM lanes 32 (w % 4) .. +31 (lane
+    // L = 32 (w % 4) + lane); sub = w / 4 splits each lane's work in two.
+    const int lane_q = 32 * (warp & 3) + lane;  // TMEM lane
+    const int sub = (warp >> 2) & 1;
+    uint32_t qa[32];
     if (warp < kSoftWarps) {
-        const int r = tid & (kPrefixRows - 1);
+        // dims 64 sub .. 64 sub + 63 of row lane_q % 64
+        const int r = lane_q & (kPrefixRows - 1);
         const uint4* src = nullptr;
         if (r < rows) {
             const int mi = r / G;
             src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                 ((int64_t)mem_s[mi] * p.num_q_heads + kvh * G + r - mi * G) * D);
+                                                 ((int64_t)mem_s[mi] * p.num_q_heads + kvh * G + r - mi * G) * D) +
+                  8 * sub;
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const uint4 a = src ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
-            const uint4 b = src ? __ldg(src + 8 + k) : make_uint4(0, 0, 0, 0);
             qa[4 * k] = a.x, qa[4 * k + 1] = a.y, qa[4 * k + 2] = a.z, qa[4 * k + 3] = a.w;
-            qb[4 * k] = b.x, qb[4 * k + 1] = b.y, qb[4 * k + 2] = b.z, qb[4 * k + 3] = b.w;
         }
     }
     uint32_t tmem = 0;
@@ -316,9 +348,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         tc_fence_after();
         tmem = *reinterpret_cast<volatile uint32_t*>(smem + S::kSlotOff);
         if (warp < kSoftWarps) {
-            const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
-            tmem_st32(lane_addr + kQCol, qa);       // dims 0-63, two per column
-            tmem_st32(lane_addr + kQCol + 32, qb);  // dims 64-127
+            const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+            tmem_st32(lane_addr + kQCol + 32 * sub, qa);  // two dims per column
         }
         tc_fence_before();
         compute_sync();  // Q is in TMEM
@@ -330,16 +361,14 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ K/V loads
         const uint64_t policy = l2_policy_evict_first();
-        const int32_t* table = p.block_tables + (int64_t)gs0 * p.max_blocks_per_seq + tok0 / BS;
         const int nblk = ntok / BS;  // <= kPrefixPartitionMax / 16 = 64
-        // the partition's block ids, loaded once: block j in ids[j / 32] of lane j % 32
-        int ids[2];
         bool bad = false;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int j = 32 * k + lane;
-            ids[k] = j < nblk ? __ldg(table + j) : 0;
-            if (ids[k] < 0 || (int64_t)ids[k] >= p.num_blocks) {
+            if (j >= nblk) {
+                ids[k] = 0;
+            } else if (ids[k] < 0 || (int64_t)ids[k] >= p.num_blocks) {
                 bad = true;
                 ids[k] = 0;  // keep the shape; the outputs are zeroed later
             }
@@ -443,45 +472,56 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax
-        const int r = tid & (kPrefixRows - 1);  // the tile row this thread works on
-        const int half = tid >> 6;              // 0: tokens 0-63 of a chunk; 1: tokens 64-127
+        // Row r = L % 64 is held by lanes r and r + 64 (half = L / 64); the
+        // four threads (half, sub) of the row take chunk tokens
+        // 64 half + 32 sub .. +31 each.
+        const int r = lane_q & (kPrefixRows - 1);
+        const int half = lane_q >> 6;
+        const int tq = 64 * half + 32 * sub;  // first chunk token of this thread
         const int lim = r < rows ? min(ntok, mem_lim[r / G] - tok0) : 0;  // tokens row r attends (<= 0: none)
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         const float sl2 = p.scale_log2;
-        uint4* xbuf = reinterpret_cast<uint4*>(smem + S::kXOff);  // [8][128]
-        float l = 0.f;  // this half's share of the row sum
+        uint4* xbuf = reinterpret_cast<uint4*>(smem + S::kXOff);  // [4][256]
+        const int partner = tid ^ 64;                             // lane L ^ 64, same sub
+        float l = 0.f;  // this thread's share of the row sum
         bool ok = true;
         for (int c = 0; c < nchunks; ++c) {
             const int sb = c & 1;
-            float v[64];
+            float v[32];
             ok = __all_sync(0xffffffffu, mbar_wait(sfull0 + 8 * sb, (c >> 1) & 1));
             if (ok) {
                 tc_fence_after();
-                float a[32], b[32];
-                tmem_ld32(lane_addr + sb * kChunk + 64 * half, a);
-                tmem_ld32(lane_addr + sb * kChunk + 64 * half + 32, b);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = a[j], v[32 + j] = b[j];
+                tmem_ld32(lane_addr + sb * kChunk + tq, v);
             } else if (lane == 0) {
                 flags[2] = 1;
             }
-            const int t0 = c * kChunk + 64 * half;  // partition token of v[0]
+            const int t0 = c * kChunk + tq;  // partition token of v[0]
             float mx = -INFINITY;
+            if (ok && t0 + 32 <= lim) {  // every token valid (the common case)
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                v[j] = ok && t0 + j < lim ? v[j] * sl2 : -INFINITY;
-                mx = fmaxf(mx, v[j]);
+                for (int j = 0; j < 32; ++j) {
+                    v[j] *= sl2;
+                    mx = fmaxf(mx, v[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    v[j] = ok && t0 + j < lim ? v[j] * sl2 : -INFINITY;
+                    mx = fmaxf(mx, v[j]);
+                }
             }
-            float* xm = xch + sb * kUmmaM;
+            float* xm = xch + sb * (kSoftWarps * 32);
             xm[tid] = mx;
             softmax_sync();
             if (flags[2]) {  // every softmax thread sees the same verdict here
                 ok = false;
                 break;
             }
-            mx = fmaxf(mx, xm[tid ^ kPrefixRows]);
+            // the row's four threads: tid, tid ^ 64 (other half), tid ^ 128
+            // (other sub), tid ^ 192
+            mx = fmaxf(fmaxf(mx, xm[tid ^ 64]), fmaxf(xm[tid ^ 128], xm[tid ^ 192]));
             // raise m only when a score exceeds it by more than kLazyMargin;
-            // both threads of a row take the same decision
+            // the row's threads take the same decision
             const bool raise = mx > m_run + kLazyMargin;
             float alpha = 1.f;
             if (raise) {
@@ -490,14 +530,13 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
             }
             const float ms = m_run == -INFINITY ? 0.f : m_run;
             l *= alpha;
-            // this thread's 64 tokens as 32 columns of high parts and 32 of
+            // this thread's 32 tokens as 16 columns of high parts and 16 of
             // residuals; it keeps the ones of its own lane (lane r: high,
-            // lane r + 64: residual) and hands the others to its partner:
-            // tokens 0-63's residual goes to lane r + 64, tokens 64-127's
-            // high part to lane r
-            uint32_t keep[32];
+            // lane r + 64: residual) and hands the others to its partner on
+            // the other lane
+            uint32_t keep[16];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
+            for (int q = 0; q < 4; ++q) {
                 uint32_t send[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -510,7 +549,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                     keep[e] = half ? lw : hw;
                     send[i] = half ? hw : lw;
                 }
-                xbuf[q * kUmmaM + tid] = make_uint4(send[0], send[1], send[2], send[3]);
+                xbuf[q * (kSoftWarps * 32) + tid] = make_uint4(send[0], send[1], send[2], send[3]);
             }
             // O is rescaled once the previous chunk's product is in it
             const bool rescale = c > 0 && __any_sync(0xffffffffu, alpha != 1.f);
@@ -520,29 +559,31 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                 ok = false;
                 break;
             }
-            uint32_t recv[32];
+            uint32_t recv[16];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint4 x = xbuf[q * kUmmaM + (tid ^ kPrefixRows)];
+            for (int q = 0; q < 4; ++q) {
+                const uint4 x = xbuf[q * (kSoftWarps * 32) + partner];
                 recv[4 * q] = x.x, recv[4 * q + 1] = x.y, recv[4 * q + 2] = x.z, recv[4 * q + 3] = x.w;
             }
             tc_fence_after();
             if (rescale) {
-                // this lane's row of O (the high or the residual product)
+                // columns 64 sub .. +63 of this lane's row of O (the high or
+                // the residual product)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
                     float o[32];
-                    const uint32_t oa = lane_addr + kOCol + 32 * q;
+                    const uint32_t oa = lane_addr + kOCol + 64 * sub + 32 * q;
                     tmem_ld32(oa, o);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] *= alpha;
                     tmem_st32(oa, o);
                 }
             }
-            // P over this lane's S columns: lane r the high part of tokens
-            // 0-127, lane r + 64 the residual, two tokens per column
-            tmem_st32(lane_addr + sb * kChunk + (half ? 32 : 0), keep);  // this thread's tokens
-            tmem_st32(lane_addr + sb * kChunk + (half ? 0 : 32), recv);  // the partner's
+            // P over this lane's S columns (two tokens per column): this
+            // thread's tokens and, at the same columns of the other half, the
+            // partner's
+            tmem_st16(lane_addr + sb * kChunk + tq / 2, keep);
+            tmem_st16(lane_addr + sb * kChunk + (tq ^ 64) / 2, recv);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(pfull0 + 8 * sb);
@@ -553,65 +594,76 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
             atomicOr(flags, 2);
             record_error(p.err, PKV_DEVERR_TIMEOUT);
         }
-        xch[2 * kUmmaM + tid] = l;  // the row sum's halves, combined below
+        xch[2 * (kSoftWarps * 32) + tid] = l;  // the row sum's four shares, combined below
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
     const int fl = flags[0];
-    float* red = reinterpret_cast<float*>(smem + S::kRedOff);  // [128 lanes][kRedStride]
+    // Each row's normalised output (high + residual product) and
+    // log-sum-exp.  The residual lanes (r + 64) put their O columns in shared
+    // memory (the ring is idle now); the high lanes (r) add their own, scale
+    // the row in place and write its log-sum-exp; then every thread copies
+    // rows out, a row's 512 bytes by 32 consecutive threads.  TMEM loads are
+    // warp-collective, so every lane runs them.
+    float* red = reinterpret_cast<float*>(smem + S::kRedOff);  // [64 rows][kRedStride]
     if (warp < kSoftWarps) {
-        // every lane's O row into shared memory (the ring is idle now; the
-        // TMEM loads are warp-collective, so every lane runs them)
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+        const int er = lane_q & (kPrefixRows - 1), ehalf = lane_q >> 6;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        float o[64];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
             float v[32];
             if (!(fl & 2)) {
-                tmem_ld32(lane_addr + kOCol + 32 * q, v);
+                tmem_ld32(lane_addr + kOCol + 64 * sub + 32 * q, v);
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.f;
             }
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(red + tid * kRedStride + 32 * q + j) =
-                    make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            for (int j = 0; j < 32; ++j) o[32 * q + j] = v[j];
+        }
+        float* row = red + er * kRedStride + 64 * sub;
+        if (ehalf) {
+#pragma unroll
+            for (int j = 0; j < 64; j += 4)
+                *reinterpret_cast<float4*>(row + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+        }
+        softmax_sync();
+        if (!ehalf) {
+            const float* ls = xch + 2 * (kSoftWarps * 32);
+            const float lsum = (ls[tid] + ls[tid ^ 64]) + (ls[tid ^ 128] + ls[tid ^ 192]);
+            const float inv = fl != 0 || !(lsum > 0.f) ? 0.f : 1.f / lsum;  // bad metadata: zeros
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+                const float4 b4 = *reinterpret_cast<const float4*>(row + j);
+                *reinterpret_cast<float4*>(row + j) = make_float4((o[j] + b4.x) * inv, (o[j + 1] + b4.y) * inv,
+                                                                  (o[j + 2] + b4.z) * inv, (o[j + 3] + b4.w) * inv);
+            }
+            const int mi = er / G;
+            if (sub == 0 && er < rows && tok0 < mem_lim[mi] && mem_np[mi] > 1) {
+                const int64_t idx = ((int64_t)mem_s[mi] * p.num_q_heads + kvh * G + er - mi * G) * p.max_parts + part;
+                p.part_lse[idx] = fl != 0 ? INFINITY : m_run + log2f(lsum);
+            }
         }
     }
     __syncthreads();
-    if (warp < kSoftWarps) {
-        // each row's normalised output (high + residual product) and
-        // log-sum-exp; thread r writes dims 0-63 of row r, thread r + 64 dims 64-127
-        const int r = tid & (kPrefixRows - 1), half = tid >> 6, mi = r / G;
-        const bool has = r < rows && tok0 < mem_lim[mi];  // row r's member has prefix tokens here
-        if (has) {
-            const bool bad = fl != 0;
-            const int s = mem_s[mi], h = kvh * G + r - mi * G;
-            const bool partial = mem_np[mi] > 1;
+    // rows of members with prefix tokens here: partials (several partitions
+    // in all) or the output itself
+    for (int i = tid; i < rows * (D / 4); i += blockDim.x) {
+        const int er = i / (D / 4), c4 = i - er * (D / 4), mi = er / G;
+        if (tok0 >= mem_lim[mi]) continue;
+        const int s = mem_s[mi], h = kvh * G + er - mi * G;
+        const float4 v = *reinterpret_cast<const float4*>(red + er * kRedStride + 4 * c4);
+        if (mem_np[mi] > 1) {
             const int64_t idx = ((int64_t)s * p.num_q_heads + h) * p.max_parts + part;
-            const float lsum = xch[2 * kUmmaM + r] + xch[2 * kUmmaM + r + kPrefixRows];
-            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            const float* hi_row = red + r * kRedStride + 64 * half;
-            const float* lo_row = red + (r + kPrefixRows) * kRedStride + 64 * half;
-            for (int j = 0; j < 64; j += 4) {
-                const float4 a4 = *reinterpret_cast<const float4*>(hi_row + j);
-                const float4 b4 = *reinterpret_cast<const float4*>(lo_row + j);
-                float4 o = make_float4((a4.x + b4.x) * inv, (a4.y + b4.y) * inv, (a4.z + b4.z) * inv,
-                                       (a4.w + b4.w) * inv);
-                if (bad) o = make_float4(0.f, 0.f, 0.f, 0.f);
-                const int d = 64 * half + j;
-                if (partial) {
-                    *reinterpret_cast<float4*>(p.part_o + idx * D + d) = o;
-                } else {
-                    store_out(p, s, h, d, o.x);
-                    store_out(p, s, h, d + 1, o.y);
-                    store_out(p, s, h, d + 2, o.z);
-                    store_out(p, s, h, d + 3, o.w);
-                }
-            }
-            if (partial && half == 0) p.part_lse[idx] = bad ? INFINITY : m_run + log2f(lsum);
+            *reinterpret_cast<float4*>(p.part_o + idx * D + 4 * c4) = v;
+        } else {
+            store_out(p, s, h, 4 * c4, v.x);
+            store_out(p, s, h, 4 * c4 + 1, v.y);
+            store_out(p, s, h, 4 * c4 + 2, v.z);
+            store_out(p, s, h, 4 * c4 + 3, v.w);
         }
     }
     tc_fence_before();
