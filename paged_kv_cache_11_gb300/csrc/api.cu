@@ -468,9 +468,11 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
     }
     int launches = 0;
     cudaError_t e = cudaSuccess;
-    if (grp && prefix_parts > 0 && grp->num_groups > 0)
+    if (grp && prefix_parts > 0 && grp->num_groups > 0) {
         e = launch_group_prefix(p, cache->dtype, cache->block_size, tmk4, tmv4, static_cast<cudaStream_t>(stream),
                                 &launches);
+        p.early_inputs = fused_append ? 0 : 1;  // the prefix kernel releases the decode kernel after its own wait
+    }
     if (e == cudaSuccess)
         e = launch_decode(p, cache->dtype, cache->block_size, tmk, tmv, static_cast<cudaStream_t>(stream), &launches);
     g_launches += launches;

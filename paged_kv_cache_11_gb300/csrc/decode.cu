@@ -102,13 +102,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
     // Launched with programmatic stream serialisation: the previous kernel on
     // the stream (e.g. the block write) may still be running.  Let the next
     // kernel start launching, then wait for the previous one to finish before
-    // reading anything it may have written.
+    // reading anything it may have written.  In a grouped call whose prefix
+    // kernel ran first (early_inputs), that kernel released this one only
+    // after the kernels before the call had completed: the inputs are read at
+    // once, and the wait comes before the first read of the prefix kernel's
+    // results.
     pdl_launch_dependents();
     if (tid == 32 * NCW) {
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
     }
-    pdl_wait();
+    const bool early = kPrefix && p.early_inputs;
+    if (!early) pdl_wait();
 
     int L, tok0, nparts, pidx, narrive, part;
     bool shared = false;  // grouped decode: s has a shared prefix; its group is checked before the epilogue
@@ -122,6 +127,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
             // group attended: zeros.  (L == prefix > 0 and attended: the
             // prefix kernel wrote it.)
             if (part == 0) {
+                if (early) pdl_wait();
                 int err = sp.err;
                 if (!err && sp.plen > 0 && !group_verified(p, s)) err = PKV_DEVERR_GROUP;
                 if (err || sp.L == 0) {
@@ -245,10 +251,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
                 __syncwarp();
             }
         }
-        if constexpr (kPrefix) {
-            // off the streaming path: every load of the partition is issued
-            if (shared && lane == 0 && !group_verified(p, s)) flags[2] = 1;
-        }
     } else {
         // ------------------------------------------------------------ consumers
         QFrag<NH> qf;
@@ -273,6 +275,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
         }
         acc_finish(acc);
     }
+    if (early) pdl_wait();  // the prefix kernel's group hints and partials are read below
     __syncthreads();
 
     const int fl = flags[0];
@@ -283,6 +286,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
             const int last_round = (issued - 1 - st) / NST;
             mbar_wait(full0 + 8 * st, last_round & 1);
         }
+    }
+    if constexpr (kPrefix) {
+        if (shared && tid == 0 && !group_verified(p, s)) flags[2] = 1;
     }
     __syncthreads();
     if constexpr (kPrefix) {

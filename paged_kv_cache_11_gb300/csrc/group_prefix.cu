@@ -232,12 +232,16 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     const int g = blockIdx.z;
     const int G = p.group;
 
-    pdl_launch_dependents();
     if (tid == 32 * kTmaWarp) {
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
     }
+    // Launched with programmatic stream serialisation.  Wait for the kernels
+    // before the call, then let the decode kernel start: it reads the call's
+    // inputs at once and waits for this kernel only before reading what this
+    // kernel writes.
     pdl_wait();
+    pdl_launch_dependents();
 
     int* mem_s = reinterpret_cast<int*>(smem + S::kMemOff);   // [64]
     int* mem_lim = mem_s + kPrefixRows;                       // [64]

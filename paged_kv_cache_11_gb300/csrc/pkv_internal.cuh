@@ -83,6 +83,11 @@ struct DecodeParams {
     int members_per_tile;           // group members per prefix CTA (whole members, <= 64 query rows)
     int row_tiles;                  // prefix CTAs per (group, KV head, prefix partition)
     int parts_in_x;                 // plain decode with > 65535 partitions: partition index in grid x
+    // grouped decode: the prefix kernel ran first and let this kernel start
+    // only once the kernels before the call had completed, so the decode
+    // kernel reads its inputs at once and waits for the prefix kernel only
+    // before it reads what that kernel writes (group hints, partials)
+    int early_inputs;
 };
 
 // Prefix partitions of grouped decode (tokens): chosen per call between the
