@@ -265,7 +265,7 @@ def decode_algorithmic_bytes(wl, fused: bool = False, groups=None) -> int:
     if groups is not None:
         gs, pl = groups
         shared = int(pl.sum()) // bs - sum(int(pl[a]) // bs for a in gs[:-1] if a < len(pl))
-        return wl.unique_kv_bytes() + q + out + (blocks - shared) * 4 + wl.num_seqs * 8 + len(gs) * 4
+        return wl.unique_kv_bytes() + q + out + (blocks - shared) * 4 + wl.num_seqs * 8 + len(gs) * 4 + extra
     return wl.kv_bytes() + q + out + blocks * 4 + wl.num_seqs * 4 + extra
 
 
@@ -378,11 +378,13 @@ def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool)
     mcl = wl.max_context_len
 
     # A decode step that appends one token per sequence, at its last position,
-    # runs as one fused launch (block write + attention); other steps (with
-    # copy-on-write copies) run copy_blocks, paged_kv_append, decode -- the
-    # grouped decode when the batch holds forked groups.
-    fused = (not args.unfused) and cow is None and np.array_equal(wl.append_seq, np.arange(wl.num_seqs))
-    grouped = bool(spec.groups) and not args.ungrouped and not fused
+    # runs the block write inside the decode call (paged_attention_append_decode,
+    # or its grouped form when the batch holds forked groups), after the step's
+    # copy-on-write copies if it has any; other steps run copy_blocks,
+    # paged_kv_append and the decode call.
+    fused = (not args.unfused) and np.array_equal(wl.append_seq, np.arange(wl.num_seqs))
+    grouped = bool(spec.groups) and not args.ungrouped
+    one_call = fused and cow is None  # the step is the decode call alone
     g_starts = g_plen = gs_d = pl_d = None
     if grouped:
         g_starts, g_plen, g_max = W.prefix_groups(wl)
@@ -395,30 +397,29 @@ def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool)
                                                    args.partition_size)
     wsp = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
 
-    def decode(q_, bt_, cl_, out_, ws_, gs_=None, pl_=None):
-        if grouped:
+    def decode(q_, bt_, cl_, out_, ws_, gs_=None, pl_=None, nk_=None, nv_=None, sm_=None):
+        """The decode call (with the block write inside it when fused)."""
+        kw = dict(out=out_, max_context_len=mcl, partition_size=args.partition_size, workspace=ws_)
+        if grouped and fused:
+            pkv.paged_attention_append_decode_grouped(q_, nk_, nv_, sm_, kc, vc, bt_, cl_, gs_, pl_, wl.scale,
+                                                      max_group_size=g_max, max_prefix_len=g_mpl, **kw)
+        elif grouped:
             pkv.paged_attention_decode_grouped(q_, kc, vc, bt_, cl_, gs_, pl_, wl.scale, max_group_size=g_max,
-                                               max_prefix_len=g_mpl, out=out_, max_context_len=mcl,
-                                               partition_size=args.partition_size, workspace=ws_)
+                                               max_prefix_len=g_mpl, **kw)
+        elif fused:
+            pkv.paged_attention_append_decode(q_, nk_, nv_, sm_, kc, vc, bt_, cl_, wl.scale, **kw)
         else:
-            pkv.paged_attention_decode(q_, kc, vc, bt_, cl_, wl.scale, out=out_, max_context_len=mcl,
-                                       partition_size=args.partition_size, workspace=ws_)
+            pkv.paged_attention_decode(q_, kc, vc, bt_, cl_, wl.scale, **kw)
 
     def step(ev=None):
         """One step; ev = (start, end) events bracket its decode call."""
-        if fused:
-            if ev is not None:
-                ev[0].record(stream)
-            pkv.paged_attention_append_decode(q, nk, nv, sm, kc, vc, bt, cl, wl.scale, out=out, max_context_len=mcl,
-                                              partition_size=args.partition_size, workspace=wsp)
-        else:
-            if cow is not None:
-                pkv.copy_blocks(kc, vc, cow)
-            if len(wl.slot_mapping):
-                pkv.paged_kv_append(nk, nv, sm, kc, vc)
-            if ev is not None:
-                ev[0].record(stream)
-            decode(q, bt, cl, out, wsp, gs_d, pl_d)
+        if cow is not None:
+            pkv.copy_blocks(kc, vc, cow)
+        if len(wl.slot_mapping) and not fused:
+            pkv.paged_kv_append(nk, nv, sm, kc, vc)
+        if ev is not None:
+            ev[0].record(stream)
+        decode(q, bt, cl, out, wsp, gs_d, pl_d, nk, nv, sm)
         if ev is not None:
             ev[1].record(stream)
 
@@ -452,7 +453,7 @@ def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool)
     # consecutive launches overlap as they do in a serving loop and that
     # launch's duration is the step's.  A step of several launches also
     # brackets its decode call with events.
-    evs = [event_pair() for _ in range(args.steps)] if (not fused or args.flush_l2) else [None] * args.steps
+    evs = [event_pair() for _ in range(args.steps)] if (not one_call or args.flush_l2) else [None] * args.steps
     # --flush-l2: each step is bracketed by its own events and the flush runs
     # between steps, outside them
     step_evs = [event_pair() for _ in range(args.steps)] if args.flush_l2 else None
@@ -478,7 +479,7 @@ def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool)
     ms_total = t_start.elapsed_time(t_end)
     if step_evs is not None:
         ms_total = sum(a.elapsed_time(b) for a, b in step_evs)  # the steps alone, without the flushes
-    if fused and step_evs is None:
+    if one_call and step_evs is None:
         dec_avg_ms = ms_total / args.steps
     else:
         dec_avg_ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
@@ -491,7 +492,7 @@ def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool)
     # drains, so these times run slightly above the timed region's mean.
     n_stat = max(args.stat_steps, args.steps) if args.stat_steps > 0 else 0
     st_evs = [event_pair() for _ in range(n_stat)]
-    dec_evs = [event_pair() for _ in range(n_stat)] if not fused else None
+    dec_evs = [event_pair() for _ in range(n_stat)] if not one_call else None
     for i in range(n_stat):
         st_evs[i][0].record(stream)
         step(dec_evs[i] if dec_evs else None)
@@ -559,16 +560,11 @@ def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool)
         v = dviews[b]
         with torch.cuda.stream(cs):
             cs.wait_event(h2d_done[b])
-            if fused:
-                pkv.paged_attention_append_decode(v["q"], v["nk"], v["nv"], v["sm"], kc, vc, v["bt"], v["cl"],
-                                                  wl.scale, out=d_out[b], max_context_len=mcl,
-                                                  partition_size=args.partition_size, workspace=wsp2[b])
-            else:
-                if cow is not None:
-                    pkv.copy_blocks(kc, vc, v["cow"])
-                if len(wl.slot_mapping):
-                    pkv.paged_kv_append(v["nk"], v["nv"], v["sm"], kc, vc)
-                decode(v["q"], v["bt"], v["cl"], d_out[b], wsp2[b], v.get("gs"), v.get("pl"))
+            if cow is not None:
+                pkv.copy_blocks(kc, vc, v["cow"])
+            if len(wl.slot_mapping) and not fused:
+                pkv.paged_kv_append(v["nk"], v["nv"], v["sm"], kc, vc)
+            decode(v["q"], v["bt"], v["cl"], d_out[b], wsp2[b], v.get("gs"), v.get("pl"), v["nk"], v["nv"], v["sm"])
             comp_done[b].record(cs)
 
     def d2h_copy(i):
@@ -620,8 +616,9 @@ def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool)
     dec_bytes = decode_algorithmic_bytes(wl, fused, (g_starts, g_plen) if grouped else None)
     achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
     traffic = traffic_per_launch(name + ("_grouped" if grouped else ""))
-    dec_api = ("paged_attention_append_decode" if fused else
-               "paged_attention_decode_grouped" if grouped else "paged_attention_decode")
+    dec_api = ("paged_attention_append_decode_grouped" if grouped and fused else
+               "paged_attention_decode_grouped" if grouped else
+               "paged_attention_append_decode" if fused else "paged_attention_decode")
 
     # ---- the oracle on the host cores (rank 0 of a one-process run): the
     # CPU baseline, and the maximum error of the GPU output against it
@@ -655,7 +652,8 @@ def measure(name: str, args, d: Device, cpu_seconds: float, single_thread: bool)
         "config": {**describe(wl), "parallelism": f"replicas x{d.ws}" if d.ws > 1 else "single GPU",
                    "l2": ("256 MB written before every step, outside the step's timing" if args.flush_l2 else
                           f"no flush ({wl.kv_bytes() / 1e6:.0f} MB of K/V per step vs 129 MB of L2)"),
-                   "api": dec_api if fused else "copy_blocks + paged_kv_append + " + dec_api,
+                   "api": " + ".join((["copy_blocks"] if cow is not None else []) +
+                                     (["paged_kv_append"] if len(wl.slot_mapping) and not fused else []) + [dec_api]),
                    "partition_size": pkv.paged_attention_partition_size(
                        wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, mcl, args.partition_size),
                    "warmup_gpu_ms": warm_ms},

@@ -269,6 +269,31 @@ pkv_status paged_attention_decode_grouped(const void* q, const void* k_cache, co
                                           const pkv_cache_desc* cache, int32_t partition_size, void* workspace,
                                           size_t workspace_bytes, void* stream);
 
+/*
+ * A grouped decode step in one call: the block write of one new token per
+ * sequence (as paged_attention_append_decode) fused into
+ * paged_attention_decode_grouped.  The result, and the cache afterwards, are
+ * those of paged_kv_append(k_new, v_new, slot_mapping, num_seqs, ...)
+ * followed by paged_attention_decode_grouped(...), provided that each
+ * sequence's new token is its last context position and lies past its
+ * shared prefix (prefix_lens[s] < context_lens[s]; a write into a shared
+ * block is preceded by its copy, "vllm", "como funciona"): slot_mapping[s]
+ * must be the slot of position context_lens[s] - 1, or negative when
+ * sequence s has no new token.  A slot that is not that position is not
+ * written and is recorded as PKV_DEVERR_SLOT.  Arguments as for
+ * paged_attention_append_decode and paged_attention_decode_grouped.
+ */
+pkv_status paged_attention_append_decode_grouped(const void* q, const void* k_new, const void* v_new,
+                                                 const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                 const int32_t* context_lens, int32_t num_seqs,
+                                                 int32_t num_q_heads, int32_t max_context_len,
+                                                 const int32_t* group_starts, int32_t num_groups,
+                                                 int32_t max_group_size, const int32_t* prefix_lens,
+                                                 int32_t max_prefix_len, float scale, void* out, int32_t out_dtype,
+                                                 const pkv_cache_desc* cache, int32_t partition_size,
+                                                 void* workspace, size_t workspace_bytes, void* stream);
+
 /* Workspace bytes paged_attention_decode_grouped needs (0 for invalid sizes). */
 size_t paged_attention_grouped_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                                int32_t max_context_len, int32_t max_prefix_len,

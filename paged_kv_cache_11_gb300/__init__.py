@@ -10,7 +10,8 @@ mappings and copy-on-write pairs; ``workload`` builds seeded synthetic inputs.
 """
 from .binding import (  # noqa: F401
     PKV_BF16, PKV_FP16, PKV_FP32, CacheDesc, PagedKVError, cache_desc, check_device_error, compact_tokens, copy_blocks,
-    launch_count, paged_attention_append_decode, paged_attention_decode, paged_attention_decode_grouped,
+    launch_count, paged_attention_append_decode, paged_attention_append_decode_grouped, paged_attention_decode,
+    paged_attention_decode_grouped,
     paged_attention_decode_static, paged_attention_grouped_workspace_bytes, paged_attention_partition_size,
     paged_attention_plan, paged_attention_workspace_bytes, paged_kv_append, status_string, swap_blocks, version,
     wait_selftest,

@@ -80,6 +80,10 @@ def _lib() -> ctypes.CDLL:
     lib.paged_attention_decode_grouped.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, vp, i32, i32, vp, i32,
                                                    ctypes.c_float, vp, i32, desc_p, i32, vp, sz, vp]
     lib.paged_attention_decode_grouped.restype = ctypes.c_int
+    lib.paged_attention_append_decode_grouped.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, vp, i32,
+                                                          i32, vp, i32, ctypes.c_float, vp, i32, desc_p, i32, vp, sz,
+                                                          vp]
+    lib.paged_attention_append_decode_grouped.restype = ctypes.c_int
     lib.paged_attention_grouped_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.paged_attention_grouped_workspace_bytes.restype = sz
     lib.copy_blocks.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, i32, desc_p, vp]
@@ -279,6 +283,45 @@ def paged_attention_decode_grouped(q: torch.Tensor, k_cache: torch.Tensor, v_cac
         int(max_context_len), _ptr(group_starts), group_starts.numel() - 1, int(max_group_size), _ptr(prefix_lens),
         int(max_prefix_len), float(scale), _ptr(out), _DTYPE_CODE.get(out.dtype, -1), ctypes.byref(desc),
         int(partition_size), _ptr(workspace), ws_bytes, _stream(stream)), "paged_attention_decode_grouped")
+    return out
+
+
+def paged_attention_append_decode_grouped(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                          slot_mapping: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                          block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                          group_starts: torch.Tensor, prefix_lens: torch.Tensor, scale: float,
+                                          max_group_size: int, max_prefix_len: int, out: torch.Tensor | None = None,
+                                          max_context_len: int | None = None, partition_size: int = 0,
+                                          workspace: torch.Tensor | None = None,
+                                          out_dtype: torch.dtype = torch.float32, stream=None) -> torch.Tensor:
+    """One grouped decode step in one call: write sequence s's new token (k_new[s], v_new[s]) to
+    slot_mapping[s] -- the slot of its last context position, past its shared prefix -- then
+    paged_attention_decode_grouped."""
+    for t in (q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, context_lens, group_starts, prefix_lens):
+        _require(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    for t in (block_tables, context_lens, group_starts, prefix_lens):
+        _require(t.dtype == torch.int32, "block_tables, context_lens, group_starts, prefix_lens must be int32")
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == q.shape[0],
+             "slot_mapping: int64, one slot per sequence")
+    _require(q.dim() == 3 and block_tables.dim() == 2 and group_starts.dim() == 1, "bad shapes")
+    desc = cache_desc(k_cache)
+    num_seqs, hq, d = q.shape
+    max_blocks = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = max_blocks * desc.block_size
+    if out is None:
+        out = torch.empty((num_seqs, hq, d), dtype=out_dtype, device=q.device)
+    _require(out.is_cuda and out.is_contiguous(), "out must be a contiguous CUDA tensor")
+    need = paged_attention_grouped_workspace_bytes(num_seqs, hq, d, max_context_len, max_prefix_len, partition_size)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib().paged_attention_append_decode_grouped(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        max_blocks, _ptr(context_lens), num_seqs, hq, int(max_context_len), _ptr(group_starts),
+        group_starts.numel() - 1, int(max_group_size), _ptr(prefix_lens), int(max_prefix_len), float(scale),
+        _ptr(out), _DTYPE_CODE.get(out.dtype, -1), ctypes.byref(desc), int(partition_size), _ptr(workspace),
+        ws_bytes, _stream(stream)), "paged_attention_append_decode_grouped")
     return out
 
 

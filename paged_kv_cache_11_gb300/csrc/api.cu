@@ -471,7 +471,7 @@ static pkv_status decode_impl(const void* q, const void* k_new, const void* v_ne
     if (grp && prefix_parts > 0 && grp->num_groups > 0) {
         e = launch_group_prefix(p, cache->dtype, cache->block_size, tmk4, tmv4, static_cast<cudaStream_t>(stream),
                                 &launches);
-        p.early_inputs = fused_append ? 0 : 1;  // the prefix kernel releases the decode kernel after its own wait
+        p.early_inputs = 1;  // the prefix kernel releases the decode kernel after its own wait
     }
     if (e == cudaSuccess)
         e = launch_decode(p, cache->dtype, cache->block_size, tmk, tmv, static_cast<cudaStream_t>(stream), &launches);
@@ -562,6 +562,23 @@ pkv_status paged_attention_decode_grouped(const void* q, const void* k_cache, co
                                           size_t workspace_bytes, void* stream) {
     const GroupArgs grp{group_starts, num_groups, max_group_size, prefix_lens, max_prefix_len};
     return decode_impl(q, nullptr, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, num_q_heads, max_context_len, scale, out, out_dtype, cache,
+                       partition_size, workspace, workspace_bytes, stream, &grp);
+}
+
+pkv_status paged_attention_append_decode_grouped(const void* q, const void* k_new, const void* v_new,
+                                                 const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                 const int32_t* context_lens, int32_t num_seqs,
+                                                 int32_t num_q_heads, int32_t max_context_len,
+                                                 const int32_t* group_starts, int32_t num_groups,
+                                                 int32_t max_group_size, const int32_t* prefix_lens,
+                                                 int32_t max_prefix_len, float scale, void* out, int32_t out_dtype,
+                                                 const pkv_cache_desc* cache, int32_t partition_size,
+                                                 void* workspace, size_t workspace_bytes, void* stream) {
+    if (num_seqs > 0 && !k_new) return PKV_ERR_INVALID_ARG;
+    const GroupArgs grp{group_starts, num_groups, max_group_size, prefix_lens, max_prefix_len};
+    return decode_impl(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, max_blocks_per_seq,
                        context_lens, num_seqs, num_q_heads, max_context_len, scale, out, out_dtype, cache,
                        partition_size, workspace, workspace_bytes, stream, &grp);
 }

@@ -14,6 +14,7 @@ int main(void) {
         (const void*)paged_attention_workspace_bytes, (const void*)paged_attention_plan,
         (const void*)paged_attention_partition_size, (const void*)paged_attention_decode,
         (const void*)paged_attention_append_decode, (const void*)paged_attention_decode_grouped,
+        (const void*)paged_attention_append_decode_grouped,
         (const void*)paged_attention_grouped_workspace_bytes, (const void*)paged_attention_decode_static,
         (const void*)copy_blocks, (const void*)swap_blocks, (const void*)compact_tokens,
         (const void*)pkv_check_device_error, (const void*)pkv_launch_count, (const void*)pkv_wait_selftest};

@@ -28,7 +28,7 @@ def test_header_declares_the_entry_points():
     assert {"paged_kv_append", "paged_attention_decode", "copy_blocks", "paged_attention_workspace_bytes",
             "pkv_check_device_error", "pkv_status_string", "pkv_launch_count", "pkv_version",
             "paged_attention_partition_size", "paged_attention_plan", "paged_attention_append_decode",
-            "swap_blocks", "compact_tokens", "paged_attention_decode_grouped",
+            "swap_blocks", "compact_tokens", "paged_attention_decode_grouped", "paged_attention_append_decode_grouped",
             "paged_attention_grouped_workspace_bytes", "paged_attention_decode_static", "pkv_wait_selftest"} <= names
 
 

@@ -75,9 +75,66 @@ def test_shared_prefix_step(gpu, bs, step):
     assert pkv.check_device_error() == 0
 
 
+def _grouped_step(wl, gs, pl, mg, dev, fused):
+    """copy_blocks of the step's copy-on-write pairs, then either the grouped
+    call with the block write inside it, or paged_kv_append + the grouped call."""
+    dt = wl.dtype
+    kc, vc = to_dev(wl.k_cache, dt, dev), to_dev(wl.v_cache, dt, dev)
+    if len(wl.cow_pairs):
+        pkv.copy_blocks(kc, vc, _dev(wl.cow_pairs, dev))
+    nk, nv, sm = to_dev(wl.new_k, dt, dev), to_dev(wl.new_v, dt, dev), _dev(wl.slot_mapping, dev)
+    if fused:
+        out = pkv.paged_attention_append_decode_grouped(
+            to_dev(wl.q, dt, dev), nk, nv, sm, kc, vc, _dev(wl.block_tables, dev), _dev(wl.context_lens, dev),
+            _dev(gs, dev), _dev(pl, dev), wl.scale, max_group_size=mg, max_prefix_len=int(pl.max()),
+            max_context_len=wl.max_context_len)
+        torch.cuda.synchronize()
+    else:
+        pkv.paged_kv_append(nk, nv, sm, kc, vc)
+        _, _, out = run_grouped(wl, gs, pl, mg, dev, kc=kc, vc=vc)
+    return kc, vc, out
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+def test_fused_grouped_step(gpu, bs):
+    """The decode step of forked samples in two calls: the copy-on-write
+    copies, then the grouped call with each sample's new-token write inside
+    it.  Pools bit-exact against the oracle's copy + append, outputs within
+    the tolerance, and the same bits as copy + append + grouped call."""
+    wl = W.make_workload("shared_prefix", groups=4, per_group=16, prefix=512, suffix=(32, 300), seed=22,
+                         block_size=bs)
+    wl.poison()
+    gs, pl, mg = W.prefix_groups(wl)
+    kc, vc, out = _grouped_step(wl, gs, pl, mg, gpu, fused=True)
+    assert pkv.check_device_error() == 0
+    okc, ovc, ref = oracle_step(wl)
+    assert np.array_equal(to_bits(kc), okc) and np.array_equal(to_bits(vc), ovc)
+    assert max_abs_err(out, ref) <= TOL
+    _, _, sep = _grouped_step(wl, gs, pl, mg, gpu, fused=False)
+    assert torch.equal(out, sep)
+    assert pkv.check_device_error() == 0
+
+
+def test_fused_grouped_rejects_a_slot_that_is_not_the_last_position(gpu):
+    pkv.check_device_error()
+    wl = W.make_workload("shared_prefix", groups=2, per_group=4, prefix=64, suffix=(32, 100), seed=23)
+    s = next(i for i, L in enumerate(wl.context_lens) if (int(L) - 1) % 16 != 0)
+    wl.slot_mapping = wl.slot_mapping.copy()
+    wl.slot_mapping[s] -= 1  # the position before the last one, in the same block
+    gs, pl, mg = W.prefix_groups(wl)
+    kc, _, _ = _grouped_step(wl, gs, pl, mg, gpu, fused=True)
+    assert pkv.check_device_error() == 1  # PKV_DEVERR_SLOT
+    wrong = int(wl.slot_mapping[s])
+    okc = wl.k_cache.copy()
+    oracle.copy_blocks(okc, wl.v_cache.copy(), wl.cow_pairs)
+    kbits = to_bits(kc)
+    assert np.array_equal(kbits[wrong // 16, :, wrong % 16], okc[wrong // 16, :, wrong % 16])  # untouched
+
+
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["shared_prefix", "shared_prefix_prefill"])
-def test_full_size_step_sampled(gpu, name):
+@pytest.mark.parametrize("name,fused", [("shared_prefix", True), ("shared_prefix", False),
+                                        ("shared_prefix_prefill", False)])
+def test_full_size_step_sampled(gpu, name, fused):
     """The shared-prefix steps the benchmark times, at full size (16 groups x
     16 members, 1024-token prompt, 256 sequences): the 240 copy-on-write
     copies, the append (256 tokens, or the 68k-token continuation), then the
@@ -85,13 +142,9 @@ def test_full_size_step_sampled(gpu, name):
     for bit; outputs are sampled against the oracle (every group's first and
     last member, plus random rows)."""
     wl = W.make_workload(name)
-    dev, dt = gpu, wl.dtype
-    kc, vc = to_dev(wl.k_cache, dt, dev), to_dev(wl.v_cache, dt, dev)
-    pkv.copy_blocks(kc, vc, _dev(wl.cow_pairs, dev))
-    pkv.paged_kv_append(to_dev(wl.new_k, dt, dev), to_dev(wl.new_v, dt, dev), _dev(wl.slot_mapping, dev), kc, vc)
     gs, pl, mg = W.prefix_groups(wl)
     assert len(gs) - 1 == 16 and mg == 16 and (pl >= 1024).all()
-    _, _, out = run_grouped(wl, gs, pl, mg, dev, kc=kc, vc=vc)
+    kc, vc, out = _grouped_step(wl, gs, pl, mg, gpu, fused=fused)
     rng = np.random.default_rng(5)
     sel = {(int(s), int(h)) for s, h in zip(rng.integers(0, wl.num_seqs, 64), rng.integers(0, wl.num_q_heads, 64))}
     for g in range(len(gs) - 1):
