@@ -207,7 +207,7 @@ struct PrefixSmem {
     static constexpr int kDynamic = kTotal + 1024;  // slack to align the base to 1024 B
     // epilogue: the residual lanes' O rows, [64][kRedStride] floats over the K/V ring
     static constexpr int kRedOff = kKOff;
-    static_assert(kPrefixRows * kRedStride * 4 <= 2 * kRing * kStage, "O rows fit the ring");
+    static_assert(kPrefixRows * kRedStride * 4 + kPrefixRows * 12 <= 2 * kRing * kStage, "O rows fit the ring");
     static_assert(kDynamic <= 227 * 1024, "shared memory of one CTA");
 };
 
@@ -612,6 +612,10 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     // rows out, a row's 512 bytes by 32 consecutive threads.  TMEM loads are
     // warp-collective, so every lane runs them.
     float* red = reinterpret_cast<float*>(smem + S::kRedOff);  // [64 rows][kRedStride]
+    // per row: where it goes (a partial's row, or null) and whether it is the
+    // output itself (a member whose context is all prefix, in one partition)
+    float** rowdst = reinterpret_cast<float**>(red + kPrefixRows * kRedStride);  // [64]
+    int* rowout = reinterpret_cast<int*>(rowdst + kPrefixRows);                  // [64]
     if (warp < kSoftWarps) {
         const int er = lane_q & (kPrefixRows - 1), ehalf = lane_q >> 6;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -645,30 +649,39 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                 *reinterpret_cast<float4*>(row + j) = make_float4((o[j] + b4.x) * inv, (o[j + 1] + b4.y) * inv,
                                                                   (o[j + 2] + b4.z) * inv, (o[j + 3] + b4.w) * inv);
             }
-            const int mi = er / G;
-            if (sub == 0 && er < rows && tok0 < mem_lim[mi] && mem_np[mi] > 1) {
+            if (sub == 0) {
+                const int mi = er / G;
+                const bool has = er < rows && tok0 < mem_lim[mi];  // the row's member has prefix tokens here
+                const bool partial = has && mem_np[mi] > 1;
                 const int64_t idx = ((int64_t)mem_s[mi] * p.num_q_heads + kvh * G + er - mi * G) * p.max_parts + part;
-                p.part_lse[idx] = fl != 0 ? INFINITY : m_run + log2f(lsum);
+                if (partial) p.part_lse[idx] = fl != 0 ? INFINITY : m_run + log2f(lsum);
+                rowdst[er] = partial ? p.part_o + idx * D : nullptr;
+                rowout[er] = has && !partial;
             }
         }
     }
     __syncthreads();
-    // rows of members with prefix tokens here: partials (several partitions
-    // in all) or the output itself
-    for (int i = tid; i < rows * (D / 4); i += blockDim.x) {
-        const int er = i / (D / 4), c4 = i - er * (D / 4), mi = er / G;
-        if (tok0 >= mem_lim[mi]) continue;
-        const int s = mem_s[mi], h = kvh * G + er - mi * G;
-        const float4 v = *reinterpret_cast<const float4*>(red + er * kRedStride + 4 * c4);
-        if (mem_np[mi] > 1) {
-            const int64_t idx = ((int64_t)s * p.num_q_heads + h) * p.max_parts + part;
-            *reinterpret_cast<float4*>(p.part_o + idx * D + 4 * c4) = v;
-        } else {
-            store_out(p, s, h, 4 * c4, v.x);
-            store_out(p, s, h, 4 * c4 + 1, v.y);
-            store_out(p, s, h, 4 * c4 + 2, v.z);
-            store_out(p, s, h, 4 * c4 + 3, v.w);
+    // Rows out, a row's 512 bytes by 32 consecutive threads; every shared
+    // load of a thread is issued before its stores.
+    constexpr int kOutIters = (kPrefixRows * (D / 4) + kPrefixThreads - 1) / kPrefixThreads;
+#pragma unroll
+    for (int k = 0; k < kOutIters; ++k) {
+        const int i = tid + k * kPrefixThreads, er = i / (D / 4), c4 = i % (D / 4);
+        if (er < rows) {
+            float* dst = rowdst[er];
+            if (dst) *reinterpret_cast<float4*>(dst + 4 * c4) = *reinterpret_cast<const float4*>(red + er * kRedStride + 4 * c4);
         }
+    }
+    // members whose whole context is prefix, in one partition: the output itself
+    for (int i = tid; i < rows * (D / 4); i += blockDim.x) {
+        const int er = i / (D / 4), c4 = i % (D / 4);
+        if (!rowout[er]) continue;
+        const int mi = er / G, s = mem_s[mi], h = kvh * G + er - mi * G;
+        const float4 v = *reinterpret_cast<const float4*>(red + er * kRedStride + 4 * c4);
+        store_out(p, s, h, 4 * c4, v.x);
+        store_out(p, s, h, 4 * c4 + 1, v.y);
+        store_out(p, s, h, 4 * c4 + 2, v.z);
+        store_out(p, s, h, 4 * c4 + 3, v.w);
     }
     tc_fence_before();
     __syncthreads();
