@@ -262,6 +262,41 @@ def test_random_groups(gpu, seed):
         assert float((plain - out).abs().max()) <= 2e-5
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_random_groups_fused_write(gpu, seed):
+    """The random group layouts as a decode step: every sequence whose last
+    position lies past its shared prefix writes its new token there inside
+    the grouped call (the others have no new token this step)."""
+    c = _case(700 + seed)
+    wl, gs, pl, mg = W.make_grouped_workload(seed, c["members"], c["hkv"] * c["G"], c["hkv"], c["bs"], c["dtype"])
+    bs = c["bs"]
+    slots = np.full(wl.num_seqs, -1, dtype=np.int64)
+    for s in range(wl.num_seqs):
+        L = int(wl.context_lens[s])
+        if L > int(pl[s]):
+            slots[s] = int(wl.block_tables[s, (L - 1) // bs]) * bs + (L - 1) % bs
+    wl.slot_mapping = slots
+    wl.append_seq = np.arange(wl.num_seqs, dtype=np.int32)
+    wl.new_k = W.normal(seed, W.S_NEW_K, (wl.num_seqs, c["hkv"], 128), c["dtype"])
+    wl.new_v = W.normal(seed, W.S_NEW_V, (wl.num_seqs, c["hkv"], 128), c["dtype"])
+    wl.poison()
+    dev, dt = gpu, wl.dtype
+    kc, vc = to_dev(wl.k_cache, dt, dev), to_dev(wl.v_cache, dt, dev)
+    out = pkv.paged_attention_append_decode_grouped(
+        to_dev(wl.q, dt, dev), to_dev(wl.new_k, dt, dev), to_dev(wl.new_v, dt, dev), _dev(slots, dev), kc, vc,
+        _dev(wl.block_tables, dev), _dev(wl.context_lens, dev), _dev(gs, dev), _dev(pl, dev), wl.scale,
+        max_group_size=mg, max_prefix_len=int(pl.max()), max_context_len=wl.max_context_len,
+        partition_size=c["P"], out_dtype=c["out_dtype"])
+    torch.cuda.synchronize()
+    assert pkv.check_device_error() == 0
+    okc, ovc, ref = oracle_step(wl)
+    assert np.array_equal(to_bits(kc), okc) and np.array_equal(to_bits(vc), ovc)
+    o = out.float().cpu().numpy()
+    assert np.isfinite(o).all(), c
+    err = np.abs(o - ref)
+    assert (err <= _tol(c["out_dtype"], ref)).all(), (c, float(err.max()))
+
+
 def test_many_prefix_partitions_use_the_merge_kernel(gpu):
     """17 prefix partitions + the own tokens: more than the in-kernel merge takes."""
     wl, gs, pl, mg = W.make_grouped_workload(7, [[(4352, 4400), (4352, 4500), (4096, 4097)], [(0, 900)]], 16, 4, 16,
