@@ -63,6 +63,26 @@ def test_long_context_small(gpu):
     _check(wl, gpu)
 
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_many_short_sequences(gpu, fused):
+    """6000 sequences of 0-70 tokens: a grid with thousands of sequence rows,
+    mostly one or two blocks each, through the separate and the fused step."""
+    wl = W.make_workload("llama8b", num_seqs=6000, lens=("uniform", 0, 70), seed=31)
+    assert (wl.context_lens == 0).any() and wl.max_context_len <= 70
+    if fused:
+        assert single_token_step(wl) is False  # empty sequences append nothing
+        live = wl.context_lens > 0
+        slots = np.full(wl.num_seqs, -1, dtype=np.int64)
+        slots[wl.append_seq] = wl.slot_mapping
+        nk = np.zeros((wl.num_seqs,) + wl.new_k.shape[1:], dtype=wl.new_k.dtype)
+        nv = np.zeros_like(nk)
+        nk[wl.append_seq], nv[wl.append_seq] = wl.new_k, wl.new_v
+        assert live.sum() == len(wl.slot_mapping)
+        wl.slot_mapping, wl.new_k, wl.new_v = slots, nk, nv
+        wl.append_seq = np.arange(wl.num_seqs, dtype=np.int32)
+    _check(wl, gpu, fused=fused)
+
+
 # ------------------------------------------------------------------ edge cases
 @pytest.mark.parametrize("lens", [(0, 1, 16, 17), (1,), (32, 31, 33, 2)])
 @pytest.mark.parametrize("bs", [16, 32])
