@@ -58,7 +58,8 @@ struct DecodeSmem {
     static constexpr int kHalfBytes = kTileBytes / 2;     // its 64-column half
     static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
     static constexpr int kStagesBytes = NST * kStageBytes;
-    static constexpr int kRedBytes = NCW * HT * kRedStride * 4 + NCW * HT * 2 * 4;
+    // per-warp rows, per-warp (m, l), per-row merge weights and lse
+    static constexpr int kRedBytes = NCW * HT * kRedStride * 4 + NCW * HT * 2 * 4 + HT * (NCW + 1) * 4;
     // the merge buffer reuses the ring once every stage has been consumed
     static constexpr int kRingBytes = ((kStagesBytes > kRedBytes ? kStagesBytes : kRedBytes) + 1023) / 1024 * 1024;
     static constexpr int kBarOffset = kRingBytes;
@@ -114,6 +115,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
     }
     const bool early = kPrefix && p.early_inputs;
     if (!early) pdl_wait();
+    // A single-pass call (every sequence one partition) starts every CTA's
+    // blocks at the sequence's first: the producer loads the first 32 block
+    // ids together with the context length, not after it.
+    const bool first_ids = !kPrefix && !p.split && warp == NCW;
+    int id0 = 0;
+    if (first_ids && lane < p.max_blocks_per_seq)
+        id0 = __ldg(p.block_tables + (int64_t)s * p.max_blocks_per_seq + lane);
 
     int L, tok0, nparts, pidx, narrive, part;
     bool shared = false;  // grouped decode: s has a shared prefix; its group is checked before the epilogue
@@ -221,7 +229,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
             int id = 0;
             bool bad = false;
             if (j < nblk) {
-                id = __ldg(table + j);
+                id = first_ids && c == 0 ? id0 : __ldg(table + j);
                 bad = id < 0 || (int64_t)id >= p.num_blocks;
                 if (bad) id = 0;  // keep the pipeline's shape; the output is zeroed later
             }
@@ -303,11 +311,47 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
         }
     }
 
-    // ---- merge the per-warp states (stage memory is free now)
+    // ---- merge the per-warp states (stage memory is free now).  Warp w's
+    // state (O_w, m_w, l_w) counts 2^(m_w - M) of the row, M = max_w m_w: the
+    // row's output is sum_w f_w O_w / sum_w f_w l_w with f_w = 2^(m_w - M).
+    // The per-row weights f_w / sum are found once, then every output
+    // element is a weighted sum of the warps' rows, a float4 at a time.
     float* red = reinterpret_cast<float*>(smem);      // [NCW][HT][kRedStride]
     float* ml = red + NCW * HT * kRedStride;           // [NCW][HT][2]
+    float* wts = ml + NCW * HT * 2;                    // [HT][NCW + 1]: weights, then the row's lse
     if (warp < NCW) acc_to_smem(acc, red, ml, warp, rows, lane);
     __syncthreads();
+    if (tid < rows) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, ml[(w * HT + tid) * 2]);
+        float f[NCW], lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+            const float mw = ml[(w * HT + tid) * 2];
+            f[w] = mw == -INFINITY ? 0.f : exp2f(mw - M);
+            lsum += f[w] * ml[(w * HT + tid) * 2 + 1];
+        }
+        const float inv = 1.f / lsum;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) wts[tid * (NCW + 1) + w] = f[w] * inv;
+        wts[tid * (NCW + 1) + NCW] = M + log2f(lsum);
+    }
+    __syncthreads();
+    // this partition's normalised output, float4 c4 of row hr
+    auto own_out = [&](int hr, int c4) {
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+            const float ww = wts[hr * (NCW + 1) + w];
+            const float4 r = *reinterpret_cast<const float4*>(red + (w * HT + hr) * kRedStride + 4 * c4);
+            o.x += ww * r.x;
+            o.y += ww * r.y;
+            o.z += ww * r.z;
+            o.w += ww * r.w;
+        }
+        return o;
+    };
 
     const bool bad = fl != 0;
     if constexpr (kPrefix) {
@@ -329,12 +373,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
                         lj[j] = __ldcg(plse + j);
                         vj[j] = __ldcg(po + j * (D / 4));
                     }
-                float lse;
-                float4 o;
-                o.x = combine_warps<NCW, HT>(red, ml, hr, 4 * c4, lse);
-                o.y = combine_warps<NCW, HT>(red, ml, hr, 4 * c4 + 1, lse);
-                o.z = combine_warps<NCW, HT>(red, ml, hr, 4 * c4 + 2, lse);
-                o.w = combine_warps<NCW, HT>(red, ml, hr, 4 * c4 + 3, lse);
+                const float lse = wts[hr * (NCW + 1) + NCW];
+                const float4 o = own_out(hr, c4);
                 float M = lse;
 #pragma unroll
                 for (int j = 0; j < MP; ++j)
@@ -354,26 +394,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
                         acc.w += wj * vj[j].w;
                     }
                 const float inv = zero ? 0.f : 1.f / sum;
-                store_out(p, s, h0 + hr, 4 * c4, acc.x * inv);
-                store_out(p, s, h0 + hr, 4 * c4 + 1, acc.y * inv);
-                store_out(p, s, h0 + hr, 4 * c4 + 2, acc.z * inv);
-                store_out(p, s, h0 + hr, 4 * c4 + 3, acc.w * inv);
+                store_out4(p, s, h0 + hr, 4 * c4, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
             }
             return;
         }
     }
-    for (int i = tid; i < rows * D; i += blockDim.x) {
-        const int hr = i / D, d = i % D;
-        float lse;
-        const float o = combine_warps<NCW, HT>(red, ml, hr, d, lse);
+    for (int i = tid; i < rows * (D / 4); i += blockDim.x) {
+        const int hr = i / (D / 4), c4 = i - hr * (D / 4);
         const int h = h0 + hr;
+        const float4 o = bad ? make_float4(0.f, 0.f, 0.f, 0.f) : own_out(hr, c4);
         if (write_partial) {
             const int64_t idx = ((int64_t)s * p.num_q_heads + h) * p.max_parts + pidx;
-            p.part_o[idx * D + d] = bad ? 0.f : o;
+            *reinterpret_cast<float4*>(p.part_o + idx * D + 4 * c4) = o;
             // +inf marks a partition whose metadata was bad: the merge zeroes the output.
-            if (d == 0) p.part_lse[idx] = bad ? INFINITY : lse;
+            if (c4 == 0) p.part_lse[idx] = bad ? INFINITY : wts[hr * (NCW + 1) + NCW];
         } else {
-            store_out(p, s, h, d, bad ? 0.f : o);
+            store_out4(p, s, h, 4 * c4, o);
         }
     }
 

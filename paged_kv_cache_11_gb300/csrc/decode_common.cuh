@@ -46,6 +46,23 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int s, int h, i
         static_cast<__half*>(p.out)[i] = __float2half_rn(v);
 }
 
+// Four consecutive output elements d .. d + 3 (d a multiple of 4) of query
+// head h of sequence s; the output is 16-byte aligned.
+__device__ __forceinline__ void store_out4(const DecodeParams& p, int s, int h, int d, float4 v) {
+    const int64_t i = ((int64_t)s * p.num_q_heads + h) * kHeadDim + d;
+    if (p.out_dtype == PKV_FP32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + i) = v;
+    } else if (p.out_dtype == PKV_BF16) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + i) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    } else {
+        const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+        *reinterpret_cast<uint2*>(static_cast<__half*>(p.out) + i) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    }
+}
+
 // Count one arrival of this call (epoch) on a (epoch << 16 | count) counter
 // and report whether it was the nparts-th.  A counter left by another call
 // (different epoch) counts as zero, so stale or garbage contents never
@@ -114,10 +131,7 @@ static __device__ __noinline__ void merge_row_partials(const DecodeParams& p, in
                 acc.w += wj * v[j].w;
             }
         const float inv = w[rows * MP + r];
-        store_out(p, s, h0 + r, 4 * c, acc.x * inv);
-        store_out(p, s, h0 + r, 4 * c + 1, acc.y * inv);
-        store_out(p, s, h0 + r, 4 * c + 2, acc.z * inv);
-        store_out(p, s, h0 + r, 4 * c + 3, acc.w * inv);
+        store_out4(p, s, h0 + r, 4 * c, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
     }
 }
 
@@ -443,27 +457,6 @@ __device__ __forceinline__ void acc_to_smem(const WarpAcc<NH>& a, float* red, fl
             }
         }
     }
-}
-
-// Merge the NCW warp states of query row hr, column d: returns the
-// normalised output and sets lse = log2-domain log-sum-exp of the row.
-template <int NCW, int HT>
-__device__ __forceinline__ float combine_warps(const float* red, const float* ml, int hr, int d, float& lse) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NCW; ++w) M = fmaxf(M, ml[(w * HT + hr) * 2]);
-    float lsum = 0.f, o = 0.f;
-#pragma unroll
-    for (int w = 0; w < NCW; ++w) {
-        const float mw = ml[(w * HT + hr) * 2];
-        if (mw != -INFINITY) {
-            const float f = exp2f(mw - M);
-            lsum += f * ml[(w * HT + hr) * 2 + 1];
-            o += f * red[(w * HT + hr) * kRedStride + d];
-        }
-    }
-    lse = M + log2f(lsum);
-    return o / lsum;
 }
 
 }  // namespace pkv
