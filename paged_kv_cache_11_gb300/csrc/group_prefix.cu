@@ -693,15 +693,19 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         // a partial from this partition; the last arrival merges the row.
         // (Members with partitions of their own are merged by the decode
         // kernel, which folds these partials in or counts them.)
+        // The partials every thread wrote before the barrier are released by
+        // the arriving thread's fence; an arrival that is last acquires the
+        // other partitions' before the barrier that starts the merges.
         const int units = nmem * p.head_tiles;
-        __threadfence();
         __syncthreads();
         for (int u = tid; u < units; u += blockDim.x) {
             const int mi = u / p.head_tiles, ht = u - mi * p.head_tiles;
             bool last = false;
             if (tok0 < mem_lim[mi] && mem_np[mi] > 1 && mem_arrive[mi]) {
                 const int64_t c = (int64_t)mem_s[mi] * p.num_kv_heads * p.head_tiles + kvh * p.head_tiles + ht;
+                fence_acq_rel_gpu();
                 last = arrive_last(p.merge_ctr + c, p.epoch, mem_np[mi]);
+                if (last) fence_acq_rel_gpu();
             }
             verdict[u] = last ? 1 : 0;
         }
@@ -710,7 +714,6 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         for (int u = 0; u < units; ++u) {
             if (!verdict[u]) continue;
             const int mi = u / p.head_tiles, ht = u - mi * p.head_tiles;
-            __threadfence();
             merge_row_partials(p, mem_s[mi], kvh * G + ht * HT, min(HT, G - ht * HT), mem_np[mi],
                                reinterpret_cast<float*>(smem));  // the ring's start: free now
             __syncthreads();  // the scratch is reused by the next merge

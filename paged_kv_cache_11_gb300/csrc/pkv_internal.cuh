@@ -185,6 +185,12 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
+// GPU-scope acquire-release fence.  After a CTA barrier, one thread's fence
+// releases the writes every thread of the CTA made before the barrier (and,
+// after an atomic that observed other CTAs' releases, acquires theirs for the
+// threads behind the next barrier).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Allow the next kernel on the stream to start launching its CTAs.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
