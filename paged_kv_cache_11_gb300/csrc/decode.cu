@@ -332,7 +332,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
             f[w] = mw == -INFINITY ? 0.f : exp2f(mw - M);
             lsum += f[w] * ml[(w * HT + tid) * 2 + 1];
         }
-        const float inv = 1.f / lsum;
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;  // 0: no warp saw a token (a wait ran out)
 #pragma unroll
         for (int w = 0; w < NCW; ++w) wts[tid * (NCW + 1) + w] = f[w] * inv;
         wts[tid * (NCW + 1) + NCW] = M + log2f(lsum);
