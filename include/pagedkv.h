@@ -80,7 +80,7 @@ enum {
     PKV_DEVERR_PREFIX_LEN = 6,  /* grouped decode: prefix_lens[s] < 0, above context_lens[s] or
                                    max_prefix_len, or not a multiple of block_size */
     PKV_DEVERR_GROUP = 7        /* grouped decode: group_starts out of order or range, or a sequence
-                                   with a shared prefix in no group or in two */
+                                   with a shared prefix in no group or beyond max_group_size members */
 };
 
 /* Shape of one layer's paged cache (host struct, read during the call). */
@@ -254,11 +254,13 @@ pkv_status paged_attention_append_decode(const void* q, const void* k_new, const
  * paged_attention_decode, with num_q_heads / num_kv_heads <= 64 and
  * num_groups <= 65535.  Bad metadata never faults: a prefix length out of
  * range (PKV_DEVERR_PREFIX_LEN), or a sequence with a nonzero prefix length
- * that lies in no group, in two groups or in a group beyond max_group_size
- * members (PKV_DEVERR_GROUP), zeroes that sequence's output; group_starts
- * out of order or out of range skip the group (PKV_DEVERR_GROUP).  The
- * pages describe the sharing, not this kernel: the grouped read is an
- * addition of this library.
+ * that lies in no group or in a group beyond max_group_size members
+ * (PKV_DEVERR_GROUP), zeroes that sequence's output.  A group whose range
+ * is out of order or out of bounds is skipped (PKV_DEVERR_GROUP); the
+ * groups on either side of it may then overlap, and a sequence in two of
+ * them gets a finite but unspecified output.  The pages describe the
+ * sharing, not this kernel: the grouped read is an addition of this
+ * library.
  */
 pkv_status paged_attention_decode_grouped(const void* q, const void* k_cache, const void* v_cache,
                                           const int32_t* block_tables, int32_t max_blocks_per_seq,
