@@ -139,22 +139,25 @@ def _code_only(text: str) -> str:
     return "\n".join(line for line in lines if line)
 
 
-def decode_source_hash() -> str:
+def decode_source_hash(grouped: bool = False) -> str:
     """sha256[:16] over the code (comments dropped) of the sources the decode
-    kernel is built from (the workloads with a traffic figure run it alone)."""
+    kernel is built from, plus the shared-prefix kernel's for a grouped call
+    (whose traffic figure is the sum over its two kernels)."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("decode.cu", "decode_common.cuh", "pkv_internal.cuh"):
+    names = ("decode.cu", "decode_common.cuh", "pkv_internal.cuh") + (("group_prefix.cu",) if grouped else ())
+    for name in names:
         h.update(_code_only((ROOT / "paged_kv_cache_11_gb300" / "csrc" / name).read_text()).encode())
     return h.hexdigest()[:16]
 
 
 def traffic_per_launch(workload: str):
     """dram read+write bytes per decode call from the committed ncu summary, if it
-    still describes the current kernels (same source hash)."""
+    still describes the current kernels (same source hash).  A grouped call's
+    entry is named <workload>_grouped."""
     if not TRAFFIC_FILE.exists():
         return None
-    h = decode_source_hash()
+    h = decode_source_hash(grouped=workload.endswith("_grouped"))
     for line in TRAFFIC_FILE.read_text().splitlines():
         parts = line.split()
         if len(parts) >= 3 and parts[0] == workload and parts[1] == h:

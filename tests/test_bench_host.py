@@ -22,10 +22,11 @@ def test_comment_edits_keep_the_code_hash_and_code_edits_change_it():
 def test_traffic_figure_is_reported_only_for_the_code_it_was_taken_on():
     """A traffic entry is used when its key is the current decode code's hash,
     and ignored (the bench line reports null) otherwise."""
-    h = bench.decode_source_hash()
     lines = [l.split() for l in bench.TRAFFIC_FILE.read_text().splitlines() if l and not l.startswith("#")]
     assert lines and all(len(l) == 3 for l in lines)
+    assert bench.decode_source_hash(grouped=True) != bench.decode_source_hash()
     for workload, key, value in lines:
+        h = bench.decode_source_hash(grouped=workload.endswith("_grouped"))
         got = bench.traffic_per_launch(workload)
         assert (got is not None) == (key == h), (workload, key, h)
         if got is not None:
