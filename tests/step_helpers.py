@@ -6,12 +6,20 @@ paged_kv_append of the step's new tokens, then paged_attention_decode.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
 import oracle
 
 TORCH_DT = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+def case_seeds(n: int) -> range:
+    """Seeds of a randomised sweep: n, or n times PKV_SOAK for a longer soak
+    run (the first n cases are always the same)."""
+    return range(n * max(1, int(os.environ.get("PKV_SOAK", "1"))))
 
 
 def to_dev(bits: np.ndarray, dtype: str, device) -> torch.Tensor:

@@ -13,7 +13,7 @@ import torch
 import oracle
 import paged_kv_cache_11_gb300 as pkv
 from paged_kv_cache_11_gb300 import workload as W
-from tests.step_helpers import max_abs_err, oracle_step, to_bits, to_dev
+from tests.step_helpers import case_seeds, max_abs_err, oracle_step, to_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 TOL = 5e-3
@@ -242,7 +242,7 @@ def _case(seed):
     return dict(dtype=dtype, bs=bs, hkv=hkv, G=G, members=members, P=P, out_dtype=out_dtype)
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", case_seeds(24))
 def test_random_groups(gpu, seed):
     c = _case(500 + seed)
     wl, gs, pl, mg = W.make_grouped_workload(seed, c["members"], c["hkv"] * c["G"], c["hkv"], c["bs"], c["dtype"])
@@ -262,7 +262,7 @@ def test_random_groups(gpu, seed):
         assert float((plain - out).abs().max()) <= 2e-5
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", case_seeds(12))
 def test_random_groups_fused_write(gpu, seed):
     """The random group layouts as a decode step: every sequence whose last
     position lies past its shared prefix writes its new token there inside

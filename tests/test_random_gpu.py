@@ -14,7 +14,7 @@ import torch
 import oracle
 import paged_kv_cache_11_gb300 as pkv
 from paged_kv_cache_11_gb300 import workload as W
-from tests.step_helpers import gpu_step, max_abs_err, oracle_step, single_token_step, to_bits, to_dev
+from tests.step_helpers import case_seeds, gpu_step, max_abs_err, oracle_step, single_token_step, to_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 TOL = 5e-3
@@ -39,7 +39,7 @@ def _case(seed):
                 fused=fused)
 
 
-@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("seed", case_seeds(40))
 def test_random_configuration(gpu, seed):
     c = _case(1000 + seed)
     wl = W.make_workload("tiny", seed=seed, num_seqs=len(c["lens"]), lens=("fixed", c["lens"]),
