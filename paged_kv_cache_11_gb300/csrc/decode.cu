@@ -11,10 +11,11 @@
 //
 // Work decomposition.  One CTA per (partition of the context, KV head, GQA
 // head tile of <= 16 query heads, sequence).  A partition is a run of
-// `partition_size` tokens (512 by default); when a sequence has more than one
-// partition, each CTA writes its normalised partial output and log-sum-exp
-// and the last partition to finish (or reduce_kernel, for many partitions)
-// merges them (split-K).  All query heads of a GQA group share one pass over
+// `partition_size` tokens (chosen per call from 512 to 4096 unless the
+// caller fixes it); when a sequence has more than one partition, each CTA
+// writes its normalised partial output and log-sum-exp and the last
+// partition to finish (or reduce_kernel, for many partitions) merges them
+// (split-K).  All query heads of a GQA group share one pass over
 // each K/V tile, so a tile is read from HBM once per KV head (once per 16
 // query heads when the group is larger than 16).  Partitions are numbered
 // from the end of each sequence and that number is the slowest grid

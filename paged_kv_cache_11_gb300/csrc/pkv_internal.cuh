@@ -94,7 +94,7 @@ struct DecodeParams {
 // smallest (which sizes the workspace) and the largest.
 constexpr int kPrefixPartition = 256;
 constexpr int kPrefixPartitionMax = 1024;
-// Resident prefix CTAs per SM (about 213 KiB of shared memory and 512 TMEM columns each).
+// Resident prefix CTAs per SM (about 214 KiB of shared memory and 512 TMEM columns each).
 constexpr int kPrefixCtasPerSm = 1;
 // Query rows of one prefix CTA (each fed twice to the prefix kernel's M = 128 products).
 constexpr int kPrefixRows = 64;
