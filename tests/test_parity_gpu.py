@@ -83,6 +83,17 @@ def test_many_short_sequences(gpu, fused):
     _check(wl, gpu, fused=fused)
 
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_maximum_batch(gpu, fused):
+    """65535 sequences, the most one call takes (one grid row each), of 1-16
+    tokens with 4 query heads on one KV head, through the separate and the
+    fused step."""
+    wl = W.make_workload("tiny", num_seqs=65535, lens=("uniform", 1, 16), num_q_heads=4, num_kv_heads=1,
+                         pool_blocks=0, seed=37)
+    assert single_token_step(wl) and wl.max_context_len == 16
+    _check(wl, gpu, fused=fused)
+
+
 # ------------------------------------------------------------------ edge cases
 @pytest.mark.parametrize("lens", [(0, 1, 16, 17), (1,), (32, 31, 33, 2)])
 @pytest.mark.parametrize("bs", [16, 32])
@@ -291,7 +302,8 @@ def test_bad_metadata_is_reported_and_zeroed(gpu):
 
 def test_host_checks(gpu):
     import paged_kv_cache_11_gb300 as pkv
-    from paged_kv_cache_11_gb300.binding import PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PagedKVError
+    from paged_kv_cache_11_gb300.binding import (PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE,
+                                                 PagedKVError)
     wl = W.make_workload("tiny")
     dev = gpu
     kc, vc = to_dev(wl.k_cache, "bf16", dev), to_dev(wl.v_cache, "bf16", dev)
@@ -308,6 +320,16 @@ def test_host_checks(gpu):
     # zero sequences: a no-op
     pkv.paged_attention_decode(q[:0], kc, vc, bt[:0], cl[:0], wl.scale)
     assert pkv.check_device_error() == 0
+    # more sequences than one call takes: refused before any launch (only the
+    # shapes are read, so the tensors are never touched)
+    n = 65536
+    qn = torch.empty((n, wl.num_q_heads, 128), dtype=torch.bfloat16, device=dev)
+    btn = torch.zeros((n, wl.block_tables.shape[1]), dtype=torch.int32, device=dev)
+    cln = torch.zeros(n, dtype=torch.int32, device=dev)
+    launches = pkv.launch_count()
+    with pytest.raises(PagedKVError) as e:
+        pkv.paged_attention_decode(qn, kc, vc, btn, cln, wl.scale, max_context_len=100)
+    assert e.value.status == PKV_ERR_INVALID_ARG and pkv.launch_count() == launches
 
 
 # ------------------------------------------------------------------ full sizes, sampled outputs
