@@ -371,6 +371,23 @@ def test_full_size_sampled(gpu, name, nsample, fused):
     assert torch.isfinite(o).all()
 
 
+@pytest.mark.slow
+def test_llama70b_long_at_512_token_partitions(gpu):
+    """llama70b_long at the split named for that workload, 512-token
+    partitions (256 per row, merged by the merge kernel), through the fused
+    step; the automatic choice above takes 4096."""
+    wl = W.make_workload("llama70b_long")
+    assert pkv.paged_attention_plan(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.block_size,
+                                    wl.max_context_len, 512) == "split+reduce"
+    kc, vc, out = gpu_step(wl, gpu, fused=True, partition_size=512)
+    sel = _sample(wl, 6, seed=1)
+    okc, ovc, ref = oracle_step(wl, select=sel, in_place=True)
+    assert np.array_equal(to_bits(kc), okc) and np.array_equal(to_bits(vc), ovc)
+    err = max_abs_err(out, ref, select=sel)
+    assert err <= TOL, err
+    assert torch.isfinite(out).all()
+
+
 # ------------------------------------------------------------------ graph capture
 @pytest.mark.parametrize("P", [0, 64])  # merge in the decode kernel / merge kernel
 def test_decode_step_captured_in_a_cuda_graph(gpu, P):
