@@ -61,7 +61,8 @@ struct DecodeParams {
     int max_blocks_per_seq;
     int len_limit;               // min(max_context_len, max_blocks_per_seq * block_size)
     int partition_size;          // tokens, multiple of block_size
-    int max_parts;               // ceil(max_context_len / partition_size), >= 1
+    int max_parts;               // partial slots per (sequence, query head): ceil(max_context_len /
+                                 // partition_size) (+ prefix_parts in grouped decode), >= 1
     int group;                   // G = Hq / Hkv
     int head_tiles;              // ceil(G / decode_head_tile(G))
     int out_dtype;               // pkv_dtype
@@ -260,18 +261,8 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
-// 2-D tiled TMA load into this CTA's shared memory, completion counted on
-// the mbarrier `bar` in bytes.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
-        : "memory");
-}
-
-// 3-D tiled TMA load (coordinates innermost first), as tma_load_2d.
+// 3-D tiled TMA load (coordinates innermost first) into this CTA's shared
+// memory, completion counted on the mbarrier `bar` in bytes.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z,
                                             uint64_t policy) {
     asm volatile(
@@ -281,7 +272,7 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// 4-D tiled TMA load (coordinates innermost first), as tma_load_2d.
+// 4-D tiled TMA load, as tma_load_3d.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z,
                                             int w, uint64_t policy) {
     asm volatile(
