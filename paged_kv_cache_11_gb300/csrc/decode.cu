@@ -437,58 +437,99 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
 
 // Split-K merge for sequences with many partitions (the decode kernel merges
 // the others itself): out = sum_p 2^(lse_p - LSE) o_p, LSE = log2 sum_p
-// 2^lse_p.  One CTA per (query head, sequence); kReduceGroups groups of 128
-// threads take interleaved partitions, thread d of a group owns column d,
-// and the groups combine through shared memory.
-constexpr int kReduceGroups = 4;
+// 2^lse_p.  One CTA per (query head, sequence).  Warp w takes partitions
+// w, w + kReduceWarps, ..., kReduceUnroll of them per round with every load
+// of the round issued together; lane l holds columns 4l .. 4l+3 as a float4.
+// Each warp keeps its own running maximum, sum and weighted output (the
+// online form of the merge), and the warps are combined in warp order
+// through shared memory, so the result depends only on the partition count.
+// The sequence's length is read beside the first round of partials, which
+// lie inside the row's workspace slots whatever the length turns out to be.
+constexpr int kReduceWarps = 8;
+constexpr int kReduceUnroll = 4;
 
-__global__ void __launch_bounds__(kHeadDim * kReduceGroups) reduce_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const DecodeParams p) {
     pdl_wait();  // the decode kernel's partials must be complete
-    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
-    const int d = tid % kHeadDim, grp = tid / kHeadDim;
+    const int h = blockIdx.x, s = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kStep = kReduceWarps * kReduceUnroll;
+    const int64_t base = ((int64_t)s * p.num_q_heads + h) * p.max_parts;
+    const float* lse = p.part_lse + base;
+    const float4* po = reinterpret_cast<const float4*>(p.part_o + base * kHeadDim) + lane;
+    // first round, before the length is known: partitions < max_parts only
+    float lj[kReduceUnroll];
+    float4 vj[kReduceUnroll];
+#pragma unroll
+    for (int u = 0; u < kReduceUnroll; ++u) {
+        const int j = warp + u * kReduceWarps;
+        if (j < p.max_parts) {
+            lj[u] = __ldcg(lse + j);
+            vj[u] = __ldcg(po + (int64_t)j * (kHeadDim / 4));
+        }
+    }
     const SeqSpan sp = seq_span(p, s, p.block_size);
     if (sp.err) return;                   // the decode kernel already zeroed it
     if (sp.plen > 0 && !group_verified(p, s)) return;
     const int np = sp.npre + sp.nsuf;
     if (np <= 1 || folds_prefix(sp)) return;  // written directly by the kernel that attended it
-    const int64_t base = ((int64_t)s * p.num_q_heads + h) * p.max_parts;
-    const float* lse = p.part_lse + base;
-    const float* po = p.part_o + base * kHeadDim + d;
-    __shared__ float red_m[kHeadDim * kReduceGroups / 32];
-    __shared__ float red_acc[kReduceGroups][kHeadDim];
-    __shared__ float red_sum[kReduceGroups];
-    // block-wide max of lse (+inf, the bad-metadata mark, wins and zeroes the row)
-    float M = -INFINITY;
-    for (int i = tid; i < np; i += blockDim.x) M = fmaxf(M, lse[i]);
+    float m = -INFINITY, l = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool bad = false;  // a partition marked +inf (bad metadata) zeroes the row
+    for (int j0 = warp;;) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if ((tid & 31) == 0) red_m[tid >> 5] = M;
-    __syncthreads();
-    M = red_m[0];
-#pragma unroll
-    for (int i = 1; i < kHeadDim * kReduceGroups / 32; ++i) M = fmaxf(M, red_m[i]);
-    if (M == INFINITY) {
-        if (grp == 0) store_out(p, s, h, d, 0.f);
-        return;
-    }
-    float acc = 0.f, sum = 0.f;
-#pragma unroll 4
-    for (int i = grp; i < np; i += kReduceGroups) {
-        const float w = exp2f(lse[i] - M);
-        sum += w;
-        acc += w * po[(int64_t)i * kHeadDim];
-    }
-    red_acc[grp][d] = acc;
-    if (d == 0) red_sum[grp] = sum;
-    __syncthreads();
-    if (grp == 0) {
-        float a = 0.f, t = 0.f;
-#pragma unroll
-        for (int g = 0; g < kReduceGroups; ++g) {
-            a += red_acc[g][d];
-            t += red_sum[g];
+        for (int u = 0; u < kReduceUnroll; ++u) {
+            const int j = j0 + u * kReduceWarps;
+            if (j < np) {
+                if (lj[u] == INFINITY) {
+                    bad = true;
+                } else if (lj[u] > -INFINITY) {
+                    const float mn = fmaxf(m, lj[u]);
+                    const float a = exp2f(m - mn), b = exp2f(lj[u] - mn);  // m = -inf: a = 0
+                    l = l * a + b;
+                    acc.x = acc.x * a + b * vj[u].x;
+                    acc.y = acc.y * a + b * vj[u].y;
+                    acc.z = acc.z * a + b * vj[u].z;
+                    acc.w = acc.w * a + b * vj[u].w;
+                    m = mn;
+                }
+            }
         }
-        store_out(p, s, h, d, a / t);
+        j0 += kStep;
+        if (j0 >= np) break;
+#pragma unroll
+        for (int u = 0; u < kReduceUnroll; ++u) {
+            const int j = j0 + u * kReduceWarps;
+            if (j < np) {
+                lj[u] = __ldcg(lse + j);
+                vj[u] = __ldcg(po + (int64_t)j * (kHeadDim / 4));
+            }
+        }
+    }
+    __shared__ float4 red_acc[kReduceWarps][kHeadDim / 4];
+    __shared__ float red_m[kReduceWarps], red_l[kReduceWarps];
+    __shared__ int red_bad;
+    if (threadIdx.x == 0) red_bad = 0;
+    __syncthreads();
+    red_acc[warp][lane] = acc;
+    if (lane == 0) {
+        red_m[warp] = m;
+        red_l[warp] = l;
+        if (bad) red_bad = 1;
+    }
+    __syncthreads();
+    if (threadIdx.x < kHeadDim) {
+        const int d = threadIdx.x;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kReduceWarps; ++w) M = fmaxf(M, red_m[w]);
+        float sum = 0.f, o = 0.f;
+#pragma unroll
+        for (int w = 0; w < kReduceWarps; ++w) {
+            const float f = exp2f(red_m[w] - M);  // a warp with no partition: m = -inf, f = 0
+            sum += f * red_l[w];
+            o += f * reinterpret_cast<const float*>(&red_acc[w][0])[d];
+        }
+        store_out(p, s, h, d, red_bad || !(sum > 0.f) ? 0.f : o / sum);
     }
 }
 
@@ -510,7 +551,7 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmk
     if (e != cudaSuccess) return e;
     ++*launches;
     if (p.split && !p.fuse_merge) {
-        e = launch_pdl(reduce_kernel, dim3(p.num_q_heads, p.num_seqs), dim3(kHeadDim * kReduceGroups), 0, stream, p);
+        e = launch_pdl(reduce_kernel, dim3(p.num_q_heads, p.num_seqs), dim3(kReduceWarps * 32), 0, stream, p);
         if (e != cudaSuccess) return e;
         ++*launches;
     }
