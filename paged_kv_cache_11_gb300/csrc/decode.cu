@@ -446,7 +446,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NH == 1 ? PKV_MINB : PKV_MINB 
 // The sequence's length is read beside the first round of partials, which
 // lie inside the row's workspace slots whatever the length turns out to be.
 constexpr int kReduceWarps = 8;
-constexpr int kReduceUnroll = 4;
+constexpr int kReduceUnroll = 8;
 
 __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const DecodeParams p) {
     pdl_wait();  // the decode kernel's partials must be complete
